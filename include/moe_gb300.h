@@ -1,0 +1,146 @@
+/*
+ * moe_gb300 -- forward pass of a gpt-oss-style sparse Mixture-of-Experts MLP
+ * layer on one GB300 (sm_103a).  Plain C ABI: device pointers, sizes, a
+ * CUDA stream passed as void*.
+ *
+ * The layer (as stated in "GPT-OSS on Day 0", perplexity.ai hub blog: the MLP
+ * bullets of the gpt-oss architecture list -- SwiGLU, softmax after top-k,
+ * experts with biases; the infrastructure decisions -- FP8 with 128x128 block
+ * scales; the MoE routing, DeepGEMM bias and combine paragraphs):
+ *
+ *   logits[t,e] = sum_h x[t,h] * router_w[e,h] + router_b[e]          (fp32)
+ *   the k largest logits (ties -> lower e), stored in ascending expert order
+ *   w[t,j]      = softmax over those k logits, rounded to bf16
+ *   rows of each expert e (tokens routed to e, ascending token order):
+ *     xq, sx    = 1x128 per-token-group FP8 e4m3 quantisation of x
+ *                 (s = amax/448, code = e4m3_rne_satfinite(x/s))
+ *     acc       = b13[e] + sum_kb sx[kb]*s13[e,n/128,kb] * (xq . w13[e,n])_kb
+ *     h         = silu(gate) * up,  requantised 1x128 -> hq, sh
+ *     y         = b2[e] + sum_kb sh[kb]*s2[e,n/128,kb] * (hq . w2[e,n])_kb
+ *   out[t,:]    = bf16( sum_j w[t,j] * y[t,j,:] )    (slot order, no atomics)
+ *
+ * Padding rule (sizes that are not multiples of 128, e.g. 2880):
+ *   Hp = ceil(H/128)*128, Ip = ceil(I/128)*128.  w13 is [E, 2*Ip, Hp] e4m3
+ *   with gate rows at [0, I) and up rows at [Ip, Ip+I); w2 is [E, Hp, Ip];
+ *   every padded row/column holds code 0; block scales cover the padded
+ *   128x128 blocks (use moe_pack_weights to build them).
+ *
+ * Ownership: the caller owns every buffer, including the workspace.  Calls
+ * never allocate device memory, never synchronise the stream (except
+ * moe_read_device_status), keep no data between calls and are asynchronous
+ * on `stream`.  Inputs are read-only; `out` is fully overwritten.
+ *
+ * Errors: arguments are checked before any launch (MOE_ERR_INVALID_ARG,
+ * MOE_ERR_UNSUPPORTED for pointers that are not 16-byte aligned or sizes
+ * beyond the limits below, MOE_ERR_WORKSPACE for a short workspace); a failed
+ * launch returns MOE_ERR_CUDA.  Every device-side wait is bounded (about 2 s);
+ * a wait that runs out stops the kernel cleanly and sets an error word in
+ * the workspace, which moe_read_device_status reports as
+ * MOE_ERR_DEVICE_TIMEOUT.
+ *
+ * Limits: 1 <= top_k <= min(E, 8); 1 <= E <= 256; 1 <= T; T*top_k < 2^31;
+ * 1 <= H, I <= 16384.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,
+    MOE_ERR_UNSUPPORTED = 2,
+    MOE_ERR_WORKSPACE = 3,
+    MOE_ERR_CUDA = 4,
+    MOE_ERR_DEVICE_TIMEOUT = 5
+} moe_status;
+
+/* Byte offsets of the intermediates inside the workspace (R = T*top_k).
+ * After moe_forward completes they hold that call's values; tests read them. */
+typedef struct {
+    size_t total_bytes;
+    size_t status;     /* uint32[64]: [0] device error word, [1] tile total GEMM1, [2] tile total GEMM2 */
+    size_t hist;       /* int32 [ceil(T/256), E] tokens per (256-token chunk, expert) + done counter */
+    size_t count;      /* int32 [E]     rows per expert */
+    size_t offset;     /* int32 [E+1]   first row of each expert (exclusive scan of count) */
+    size_t chunk_base; /* int32 [ceil(T/256), E] first row of each (chunk, expert) */
+    size_t tiles1;     /* int32 [E+1]   first gate/up GEMM tile of each expert */
+    size_t tiles2;     /* int32 [E+1]   first down GEMM tile of each expert */
+    size_t topk_idx;   /* int32 [T, top_k] selected experts, ascending */
+    size_t topk_w;     /* float [T, top_k] softmax weights before bf16 rounding */
+    size_t topk_wb;    /* bf16  [T, top_k] routing weights used by the layer */
+    size_t perm;       /* int32 [R] row r -> t*top_k + j; rows sorted by (expert, token) */
+    size_t inv;        /* int32 [R] t*top_k + j -> row */
+    size_t xq;         /* e4m3  [R, Hp] quantised x, permuted rows */
+    size_t sx;         /* float [R, Hp/128] */
+    size_t hq;         /* e4m3  [R, Ip] requantised h */
+    size_t sh;         /* float [R, Ip/128] */
+    size_t part;       /* float [R, Hp] w[t,j]*y rows, indexed by t*top_k + j */
+} moe_workspace_layout;
+
+/* Bytes of workspace moe_forward needs for these sizes (0 if the sizes are invalid). */
+size_t moe_workspace_size(int T, int H, int I, int E, int top_k);
+
+/* Fills *layout for these sizes. */
+moe_status moe_get_workspace_layout(int T, int H, int I, int E, int top_k, moe_workspace_layout* layout);
+
+/*
+ * The layer forward.
+ *   x        bf16 [T, H] row-major          router_w bf16 [E, H]    router_b bf16 [E]
+ *   w13      e4m3 [E, 2*Ip, Hp]             s13 fp32 [E, 2*Ip/128, Hp/128]
+ *   b13      bf16 [E, 2*I]  (gate [0,I), up [I,2I))
+ *   w2       e4m3 [E, Hp, Ip]               s2  fp32 [E, Hp/128, Ip/128]
+ *   b2       bf16 [E, H]
+ *   out      bf16 [T, H]
+ *   workspace: device buffer of at least moe_workspace_size(...) bytes, 256-byte aligned.
+ * All pointers are device pointers; x, w13, w2, out and the workspace must be
+ * 16-byte aligned.  stream is a cudaStream_t (NULL = legacy default stream).
+ */
+moe_status moe_forward(const void* x, const void* router_w, const void* router_b, const uint8_t* w13, const float* s13,
+                       const void* b13, const uint8_t* w2, const float* s2, const void* b2, int T, int H, int I, int E,
+                       int top_k, void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Weight packer (the offline converter from master weights to the layer's
+ * FP8 layout; "GPT-OSS on Day 0": FP8 with 128x128 block scaling).
+ *   w13_f32 fp32 [E, 2*I, H] (gate rows then up rows), w2_f32 fp32 [E, H, I]  (device)
+ *   -> w13 e4m3 [E, 2*Ip, Hp], s13 [E, 2*Ip/128, Hp/128], w2 e4m3 [E, Hp, Ip], s2 [E, Hp/128, Ip/128]
+ * Each 128x128 block: s = amax/448 (1 when the block is all zero), code =
+ * e4m3_rne_satfinite(w/s) in IEEE fp32; padding gets code 0.
+ * Either input may be NULL to pack only the other matrix.
+ */
+moe_status moe_pack_weights(const float* w13_f32, const float* w2_f32, int H, int I, int E, uint8_t* w13, float* s13,
+                            uint8_t* w2, float* s2, void* stream);
+
+/*
+ * The 1x128 group quantiser on its own (the step the gate/up GEMM epilogue
+ * applies to h, and the one applied to x): in fp32 [rows, cols] with row
+ * stride ld_in (elements) -> q e4m3 [rows, ceil(cols/128)*128],
+ * s fp32 [rows, ceil(cols/128)].  Same device arithmetic as the fused epilogue.
+ */
+moe_status moe_quantize_rows(const float* in, int rows, int cols, int ld_in, uint8_t* q, float* s, void* stream);
+
+/* Synchronises `stream`, then reads and clears the device error word of
+ * `workspace`: MOE_OK, MOE_ERR_DEVICE_TIMEOUT (a bounded wait ran out), or
+ * MOE_ERR_CUDA. */
+moe_status moe_read_device_status(void* workspace, void* stream);
+
+/*
+ * Check of the bounded-wait machinery: one thread waits on a barrier that
+ * receives `arrivals` arrivals out of the 1 it needs (0 = never completes),
+ * for at most timeout_ns.  Writes 1 (completed) or 2 (timed out) to
+ * *result_dev (device uint32).  No fault, trap or hang is possible.
+ */
+moe_status moe_test_bounded_wait(uint64_t timeout_ns, int arrivals, uint32_t* result_dev, void* stream);
+
+const char* moe_status_str(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

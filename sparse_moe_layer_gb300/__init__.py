@@ -1,0 +1,243 @@
+"""Sparse Mixture-of-Experts MLP layer forward (gpt-oss style) on GB300.
+
+Thin Python binding of the C ABI in ``include/moe_gb300.h`` (library
+``libmoe_gb300.so``, built in-tree for sm_103a).  Every step of the layer runs
+in the library's CUDA kernels; this module only checks tensors and passes
+pointers, sizes and the current CUDA stream.  There is no CPU fallback: if the
+library is missing, importing the binding's functions raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB, build
+
+__all__ = ["MoeError", "build", "lib", "workspace_size", "workspace_layout", "workspace_views", "forward",
+           "pack_weights", "quantize_rows", "read_device_status", "test_bounded_wait", "MoeLayer", "pad128"]
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "CUDA error",
+          5: "device wait timed out"}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: moe_status {code} ({STATUS.get(code, '?')})")
+        self.code = code
+
+
+_LAYOUT_FIELDS = ["total_bytes", "status", "hist", "count", "offset", "chunk_base", "tiles1", "tiles2", "topk_idx",
+                  "topk_w", "topk_wb", "perm", "inv", "xq", "sx", "hq", "sh", "part"]
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_size_t) for f in _LAYOUT_FIELDS]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"{LIB} is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB)
+        vp, i32, sz, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint64
+        L.moe_workspace_size.argtypes = [i32] * 5
+        L.moe_workspace_size.restype = sz
+        L.moe_get_workspace_layout.argtypes = [i32] * 5 + [ctypes.POINTER(_Layout)]
+        L.moe_get_workspace_layout.restype = i32
+        L.moe_forward.argtypes = [vp] * 9 + [i32] * 5 + [vp, vp, sz, vp]
+        L.moe_forward.restype = i32
+        L.moe_pack_weights.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+        L.moe_pack_weights.restype = i32
+        L.moe_quantize_rows.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+        L.moe_quantize_rows.restype = i32
+        L.moe_read_device_status.argtypes = [vp, vp]
+        L.moe_read_device_status.restype = i32
+        L.moe_test_bounded_wait.argtypes = [u64, i32, vp, vp]
+        L.moe_test_bounded_wait.restype = i32
+        L.moe_status_str.argtypes = [i32]
+        L.moe_status_str.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def pad128(n: int) -> int:
+    return (n + 127) // 128 * 128
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise MoeError(code, what)
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _dev(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def workspace_size(T: int, H: int, I: int, E: int, top_k: int) -> int:
+    return int(lib().moe_workspace_size(T, H, I, E, top_k))
+
+
+def workspace_layout(T: int, H: int, I: int, E: int, top_k: int) -> dict:
+    L = _Layout()
+    _check(lib().moe_get_workspace_layout(T, H, I, E, top_k, ctypes.byref(L)), "moe_get_workspace_layout")
+    return {f: getattr(L, f) for f in _LAYOUT_FIELDS}
+
+
+def new_workspace(T: int, H: int, I: int, E: int, top_k: int, device=None) -> torch.Tensor:
+    n = workspace_size(T, H, I, E, top_k)
+    if n == 0:
+        raise MoeError(1, "workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def workspace_views(ws: torch.Tensor, T: int, H: int, I: int, E: int, top_k: int) -> dict:
+    """Typed views of the intermediates a forward call left in `ws`."""
+    L = workspace_layout(T, H, I, E, top_k)
+    R, Hp, Ip = T * top_k, pad128(H), pad128(I)
+    nch = (T + 255) // 256
+
+    def v(name, n, dtype, shape):
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return ws[L[name]:L[name] + nbytes].view(dtype).view(shape)
+
+    return dict(
+        status=v("status", 64, torch.int32, (64,)),
+        hist=v("hist", nch * E, torch.int32, (nch, E)),
+        count=v("count", E, torch.int32, (E,)),
+        offset=v("offset", E + 1, torch.int32, (E + 1,)),
+        chunk_base=v("chunk_base", nch * E, torch.int32, (nch, E)),
+        tiles1=v("tiles1", E + 1, torch.int32, (E + 1,)),
+        tiles2=v("tiles2", E + 1, torch.int32, (E + 1,)),
+        topk_idx=v("topk_idx", R, torch.int32, (T, top_k)),
+        topk_w=v("topk_w", R, torch.float32, (T, top_k)),
+        topk_wb=v("topk_wb", R, torch.bfloat16, (T, top_k)),
+        perm=v("perm", R, torch.int32, (R,)),
+        inv=v("inv", R, torch.int32, (R,)),
+        xq=v("xq", R * Hp, torch.uint8, (R, Hp)),
+        sx=v("sx", R * Hp // 128, torch.float32, (R, Hp // 128)),
+        hq=v("hq", R * Ip, torch.uint8, (R, Ip)),
+        sh=v("sh", R * Ip // 128, torch.float32, (R, Ip // 128)),
+        part=v("part", R * Hp, torch.float32, (R, Hp)),
+    )
+
+
+def forward(x, router_w, router_b, w13, s13, b13, w2, s2, b2, top_k: int, out=None, workspace=None, stream=None):
+    """out [T, H] bf16 = the MoE layer applied to x [T, H] bf16 (see moe_forward)."""
+    T, H = x.shape
+    E = router_w.shape[0]
+    I = b13.shape[1] // 2
+    Hp, Ip = pad128(H), pad128(I)
+    if tuple(w13.shape) != (E, 2 * Ip, Hp) or tuple(w2.shape) != (E, Hp, Ip):
+        raise ValueError(f"packed weight shapes {tuple(w13.shape)}, {tuple(w2.shape)} do not match H={H} I={I} E={E}")
+    if tuple(s13.shape) != (E, 2 * Ip // 128, Hp // 128) or tuple(s2.shape) != (E, Hp // 128, Ip // 128):
+        raise ValueError("block scale shapes do not match")
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = new_workspace(T, H, I, E, top_k, x.device)
+    ptrs = [_dev(x, torch.bfloat16, "x"), _dev(router_w, torch.bfloat16, "router_w"),
+            _dev(router_b, torch.bfloat16, "router_b"), _dev(w13, torch.uint8, "w13"), _dev(s13, torch.float32, "s13"),
+            _dev(b13, torch.bfloat16, "b13"), _dev(w2, torch.uint8, "w2"), _dev(s2, torch.float32, "s2"),
+            _dev(b2, torch.bfloat16, "b2")]
+    code = lib().moe_forward(*ptrs, T, H, I, E, top_k, _dev(out, torch.bfloat16, "out"),
+                             _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
+    _check(code, "moe_forward")
+    return out
+
+
+def pack_weights(w13_f32: torch.Tensor, w2_f32: torch.Tensor, stream=None, out=None):
+    """fp32 masters w13 [E, 2I, H], w2 [E, H, I] -> (w13 e4m3 codes, s13, w2 codes, s2) in the layer's layout."""
+    E, twoI, H = w13_f32.shape
+    I = twoI // 2
+    Hp, Ip = pad128(H), pad128(I)
+    dev = w13_f32.device
+    if out is None:
+        out = (torch.empty((E, 2 * Ip, Hp), dtype=torch.uint8, device=dev),
+               torch.empty((E, 2 * Ip // 128, Hp // 128), dtype=torch.float32, device=dev),
+               torch.empty((E, Hp, Ip), dtype=torch.uint8, device=dev),
+               torch.empty((E, Hp // 128, Ip // 128), dtype=torch.float32, device=dev))
+    q13, s13, q2, s2 = out
+    if tuple(w2_f32.shape) != (E, H, I):
+        raise ValueError("w2 shape does not match w13")
+    code = lib().moe_pack_weights(_dev(w13_f32, torch.float32, "w13_f32"), _dev(w2_f32, torch.float32, "w2_f32"), H,
+                                  I, E, _dev(q13, torch.uint8, "w13"), _dev(s13, torch.float32, "s13"),
+                                  _dev(q2, torch.uint8, "w2"), _dev(s2, torch.float32, "s2"), _stream(stream))
+    _check(code, "moe_pack_weights")
+    return q13, s13, q2, s2
+
+
+def pack_weights_into(w13_f32, w2_f32, H: int, I: int, E: int, q13, s13, q2, s2, stream=None):
+    """Pack a slice of experts (either master may be None) into preallocated outputs."""
+    code = lib().moe_pack_weights(None if w13_f32 is None else _dev(w13_f32, torch.float32, "w13_f32"),
+                                  None if w2_f32 is None else _dev(w2_f32, torch.float32, "w2_f32"), H, I, E,
+                                  None if q13 is None else q13.data_ptr(), None if s13 is None else s13.data_ptr(),
+                                  None if q2 is None else q2.data_ptr(), None if s2 is None else s2.data_ptr(),
+                                  _stream(stream))
+    _check(code, "moe_pack_weights")
+
+
+def quantize_rows(v: torch.Tensor, stream=None):
+    """1x128 group quantisation of fp32 rows [rows, cols] -> (codes [rows, cols_p] u8, scales [rows, cols_p/128])."""
+    rows, cols = v.shape
+    cp = pad128(cols)
+    q = torch.empty((rows, cp), dtype=torch.uint8, device=v.device)
+    s = torch.empty((rows, cp // 128), dtype=torch.float32, device=v.device)
+    _check(lib().moe_quantize_rows(_dev(v, torch.float32, "v"), rows, cols, cols, q.data_ptr(), s.data_ptr(),
+                                   _stream(stream)), "moe_quantize_rows")
+    return q, s
+
+
+def read_device_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise and return the device status code of the last forward (0 = ok, 5 = a wait timed out)."""
+    return int(lib().moe_read_device_status(_dev(workspace, torch.uint8, "workspace"), _stream(stream)))
+
+
+def test_bounded_wait(timeout_ns: int, arrivals: int, stream=None) -> int:
+    """1 if a barrier wait completed, 2 if it gave up after timeout_ns (see moe_test_bounded_wait)."""
+    r = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _check(lib().moe_test_bounded_wait(int(timeout_ns), int(arrivals), r.data_ptr(), _stream(stream)),
+           "moe_test_bounded_wait")
+    torch.cuda.synchronize()
+    return int(r.item())
+
+
+class MoeLayer:
+    """A layer with packed weights resident on the GPU and a reusable workspace."""
+
+    def __init__(self, router_w, router_b, w13, s13, b13, w2, s2, b2, top_k: int):
+        self.router_w, self.router_b = router_w, router_b
+        self.w13, self.s13, self.b13, self.w2, self.s2, self.b2 = w13, s13, b13, w2, s2, b2
+        self.top_k = top_k
+        self.E, self.H = router_w.shape
+        self.I = b13.shape[1] // 2
+        self._ws = None
+        self._ws_T = -1
+
+    def workspace(self, T: int) -> torch.Tensor:
+        if self._ws is None or self._ws_T < T:
+            self._ws = new_workspace(T, self.H, self.I, self.E, self.top_k, self.router_w.device)
+            self._ws_T = T
+        return self._ws
+
+    def __call__(self, x: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+        T = x.shape[0]
+        return forward(x, self.router_w, self.router_b, self.w13, self.s13, self.b13, self.w2, self.s2, self.b2,
+                       self.top_k, out=out, workspace=self.workspace(T), stream=stream)

@@ -1,0 +1,291 @@
+// C ABI of the sparse MoE layer: argument checks, workspace carving, TMA
+// tensor maps and the launch sequence
+//   router -> permute + x quant -> gate/up GEMM -> down GEMM -> combine
+// all on the caller's stream, with no allocation and no synchronisation.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/moe_gb300.h"
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+using namespace moe;
+
+namespace {
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline int pad128(int v) { return (v + 127) / 128 * 128; }
+
+bool sizes_ok(int T, int H, int I, int E, int k) {
+    if (T < 1 || H < 1 || I < 1 || E < 1 || k < 1) return false;
+    if (E > kMaxExperts || k > kMaxTopK || k > E) return false;
+    if (H > 16384 || I > 16384) return false;
+    if ((long long)T * k >= (1LL << 31)) return false;
+    return true;
+}
+
+void layout_of(int T, int H, int I, int E, int k, moe_workspace_layout* L) {
+    const size_t R = (size_t)T * k;
+    const size_t Hp = pad128(H), Ip = pad128(I);
+    const size_t nch = (T + kChunkTokens - 1) / kChunkTokens;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L->status = take(kStatusWords * 4);
+    L->hist = take((nch * E + 1) * 4);  // + arrival counter
+    L->count = take((size_t)E * 4);
+    L->offset = take((size_t)(E + 1) * 4);
+    L->chunk_base = take(nch * E * 4);
+    L->tiles1 = take((size_t)(E + 1) * 4);
+    L->tiles2 = take((size_t)(E + 1) * 4);
+    L->topk_idx = take(R * 4);
+    L->topk_w = take(R * 4);
+    L->topk_wb = take(R * 2);
+    L->perm = take(R * 4);
+    L->inv = take(R * 4);
+    L->xq = take(R * Hp);
+    L->sx = take(R * (Hp / 128) * 4);
+    L->hq = take(R * Ip);
+    L->sh = take(R * (Ip / 128) * 4);
+    L->part = take(R * Hp * 4);
+    L->total_bytes = o;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+// 2D uint8 tensor [rows, cols] (row stride = cols bytes), box 128 x 128, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_size(int T, int H, int I, int E, int top_k) {
+    if (!sizes_ok(T, H, I, E, top_k)) return 0;
+    moe_workspace_layout L;
+    layout_of(T, H, I, E, top_k, &L);
+    return L.total_bytes;
+}
+
+moe_status moe_get_workspace_layout(int T, int H, int I, int E, int top_k, moe_workspace_layout* layout) {
+    if (!layout || !sizes_ok(T, H, I, E, top_k)) return MOE_ERR_INVALID_ARG;
+    layout_of(T, H, I, E, top_k, layout);
+    return MOE_OK;
+}
+
+moe_status moe_forward(const void* x, const void* router_w, const void* router_b, const uint8_t* w13, const float* s13,
+                       const void* b13, const uint8_t* w2, const float* s2, const void* b2, int T, int H, int I, int E,
+                       int top_k, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!x || !router_w || !router_b || !w13 || !s13 || !b13 || !w2 || !s2 || !b2 || !out || !workspace)
+        return MOE_ERR_INVALID_ARG;
+    if (!sizes_ok(T, H, I, E, top_k)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MOE_ERR_UNSUPPORTED;
+    moe_workspace_layout L;
+    layout_of(T, H, I, E, top_k, &L);
+    if (workspace_bytes < L.total_bytes) return MOE_ERR_WORKSPACE;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int Hp = pad128(H), Ip = pad128(I);
+    const int R = T * top_k;
+    const int nch = (T + kChunkTokens - 1) / kChunkTokens;
+    const int sms = num_sms();
+
+    // status words and the (chunk, expert) histogram start at zero
+    if (cudaMemsetAsync(ws, 0, L.count, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+    RouteParams rp;
+    rp.x = static_cast<const uint16_t*>(x);
+    rp.rw = static_cast<const uint16_t*>(router_w);
+    rp.rb = static_cast<const uint16_t*>(router_b);
+    rp.T = T;
+    rp.H = H;
+    rp.E = E;
+    rp.k = top_k;
+    rp.nchunks = nch;
+    rp.nt1 = Ip / 128;
+    rp.nt2 = Hp / 128;
+    rp.topk_idx = reinterpret_cast<int32_t*>(ws + L.topk_idx);
+    rp.topk_w = reinterpret_cast<float*>(ws + L.topk_w);
+    rp.topk_wb = reinterpret_cast<uint16_t*>(ws + L.topk_wb);
+    rp.hist = reinterpret_cast<int32_t*>(ws + L.hist);
+    rp.done = rp.hist + (size_t)nch * E;
+    rp.count = reinterpret_cast<int32_t*>(ws + L.count);
+    rp.offset = reinterpret_cast<int32_t*>(ws + L.offset);
+    rp.chunk_base = reinterpret_cast<int32_t*>(ws + L.chunk_base);
+    rp.tiles1 = reinterpret_cast<int32_t*>(ws + L.tiles1);
+    rp.tiles2 = reinterpret_cast<int32_t*>(ws + L.tiles2);
+    rp.status = reinterpret_cast<uint32_t*>(ws + L.status);
+    if (launch_router(rp, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+    PermuteParams pp;
+    pp.x = rp.x;
+    pp.T = T;
+    pp.H = H;
+    pp.Hp = Hp;
+    pp.E = E;
+    pp.k = top_k;
+    pp.tokens_per_cta = T <= 2048 ? 1 : 8;
+    pp.topk_idx = rp.topk_idx;
+    pp.chunk_base = rp.chunk_base;
+    pp.perm = reinterpret_cast<int32_t*>(ws + L.perm);
+    pp.inv = reinterpret_cast<int32_t*>(ws + L.inv);
+    pp.xq = ws + L.xq;
+    pp.sx = reinterpret_cast<float*>(ws + L.sx);
+    if (launch_permute_quant(pp, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+    // upper bound of the tile count of either GEMM: sum_e ceil(count_e/128) <= E + R/128
+    const long long mt_bound = (long long)E + (R + 127) / 128;
+
+    CUtensorMap tmA1, tmB1, tmA2, tmB2;
+    if (!make_map(&tmA1, pp.xq, R, Hp) || !make_map(&tmB1, w13, (uint64_t)E * 2 * Ip, Hp) ||
+        !make_map(&tmA2, ws + L.hq, R, Ip) || !make_map(&tmB2, w2, (uint64_t)E * Hp, Ip))
+        return MOE_ERR_CUDA;
+
+    GemmParams g1;
+    memset(&g1, 0, sizeof(g1));
+    g1.E = E;
+    g1.R = R;
+    g1.KB = Hp / 128;
+    g1.N_real = I;
+    g1.rows_B = 2 * Ip;
+    g1.up_rows = Ip;
+    g1.sw_rowblocks = 2 * Ip / 128;
+    g1.count = rp.count;
+    g1.offset = rp.offset;
+    g1.tiles = rp.tiles1;
+    g1.sa = pp.sx;
+    g1.sw = s13;
+    g1.bias = static_cast<const uint16_t*>(b13);
+    g1.hq = ws + L.hq;
+    g1.sh = reinterpret_cast<float*>(ws + L.sh);
+    g1.ldq = Ip;
+    g1.status = rp.status;
+    long long t1 = mt_bound * (Ip / 128);
+    int grid1 = (int)(t1 < sms ? t1 : sms);
+    if (launch_gemm_gateup(tmA1, tmB1, g1, grid1, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+    GemmParams g2;
+    memset(&g2, 0, sizeof(g2));
+    g2.E = E;
+    g2.R = R;
+    g2.KB = Ip / 128;
+    g2.N_real = H;
+    g2.rows_B = Hp;
+    g2.up_rows = 0;
+    g2.sw_rowblocks = Hp / 128;
+    g2.count = rp.count;
+    g2.offset = rp.offset;
+    g2.tiles = rp.tiles2;
+    g2.sa = g1.sh;
+    g2.sw = s2;
+    g2.bias = static_cast<const uint16_t*>(b2);
+    g2.perm = pp.perm;
+    g2.topk_wb = rp.topk_wb;
+    g2.part = reinterpret_cast<float*>(ws + L.part);
+    g2.ldp = Hp;
+    g2.status = rp.status;
+    long long t2 = mt_bound * (Hp / 128);
+    int grid2 = (int)(t2 < sms ? t2 : sms);
+    if (launch_gemm_down(tmA2, tmB2, g2, grid2, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+    if (launch_combine(g2.part, T, H, Hp, top_k, static_cast<uint16_t*>(out), sms, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status moe_pack_weights(const float* w13_f32, const float* w2_f32, int H, int I, int E, uint8_t* w13, float* s13,
+                            uint8_t* w2, float* s2, void* stream) {
+    if (H < 1 || I < 1 || E < 1 || H > 16384 || I > 16384 || E > kMaxExperts) return MOE_ERR_INVALID_ARG;
+    if (!w13_f32 && !w2_f32) return MOE_ERR_INVALID_ARG;
+    if ((w13_f32 && (!w13 || !s13)) || (w2_f32 && (!w2 || !s2))) return MOE_ERR_INVALID_ARG;
+    if ((w13 && !aligned16(w13)) || (w2 && !aligned16(w2))) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int Hp = pad128(H), Ip = pad128(I);
+    if (w13_f32 && launch_pack_blocks(w13_f32, E, 2 * I, H, 2 * Ip, Hp, I, w13, s13, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (w2_f32 && launch_pack_blocks(w2_f32, E, H, I, Hp, Ip, 0, w2, s2, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status moe_quantize_rows(const float* in, int rows, int cols, int ld_in, uint8_t* q, float* s, void* stream) {
+    if (!in || !q || !s || rows < 1 || cols < 1 || ld_in < cols) return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(q) & 3u) return MOE_ERR_UNSUPPORTED;
+    if (launch_quantize_rows(in, rows, cols, ld_in, q, s, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status moe_read_device_status(void* workspace, void* stream) {
+    if (!workspace) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemset(workspace, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
+    return word ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+}
+
+moe_status moe_test_bounded_wait(uint64_t timeout_ns, int arrivals, uint32_t* result_dev, void* stream) {
+    if (!result_dev || arrivals < 0 || arrivals > 1) return MOE_ERR_INVALID_ARG;
+    if (launch_bounded_wait_test(timeout_ns, arrivals, result_dev, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+const char* moe_status_str(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported (alignment or size limit)";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_CUDA: return "CUDA launch or runtime error";
+        case MOE_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

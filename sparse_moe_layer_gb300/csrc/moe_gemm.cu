@@ -1,0 +1,354 @@
+// Grouped FP8 (e4m3) expert GEMMs with 128x128 block scales on tcgen05.
+//
+// "GPT-OSS on Day 0" (perplexity.ai hub blog) serves the experts as FP8 with
+// 128x128 block scales on DeepGEMM, with the bias loaded into the
+// accumulators once per output block; this is the sm_103a counterpart:
+//
+//   acc[r, n] = bias[n] + sum_kb (sa[r, kb] * sw[n/128, kb]) * P_kb[r, n],
+//   P_kb      = sum_{k in block kb} a[r, k] * w[n, k]      (one 128-wide K block)
+//
+// tcgen05.mma (kind::f8f6f4) has no per-block fp32 scale, so each K block is
+// accumulated on its own into a TMEM buffer (ping-pong), and the epilogue
+// warps "promote" it into fp32 registers that started at the bias.
+//
+// Roles (one CTA per SM, persistent over a static tile list ordered expert,
+// n-tile, m-tile so that the m-tiles of one weight tile run side by side and
+// share it through L2):
+//   warp 0      TMA producer: A (activation rows of one expert) and B (the
+//               expert's weight rows) per K block into a STAGES-deep ring.
+//   warp 1      TMEM allocator and MMA issuer (one thread): 4 MMAs of K=32
+//               per K block into TMEM buffer kb % NBUF, then commits.
+//   warps 2-9   promotion + epilogue: tcgen05.ld the partial, FMA with the
+//               two scales into registers, release the buffer; after the last
+//               K block run the fused epilogue:
+//                 gate/up GEMM: SwiGLU + 1x128 FP8 requant -> hq, sh
+//                 down GEMM:    routing-weight scale -> part[t*k+j, :]
+// Every mbarrier wait is bounded; a timeout sets an error bit and all roles
+// drain and exit.
+#include <cuda_bf16.h>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+template <bool GATED>
+struct GemmCfg {
+    static constexpr int BM = 128;
+    static constexpr int BN = GATED ? 256 : 128;  // gate/up: 128 gate + 128 up columns of one h block
+    static constexpr int A_BYTES = BM * 128;
+    static constexpr int B_BYTES = BN * 128;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = GATED ? 4 : 6;
+    static constexpr int NBUF = 512 / BN;  // TMEM partial buffers (all 512 columns)
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int THREADS = (2 + EPI_WARPS) * 32;
+    static constexpr int COLS = BN / 2;  // accumulator columns per epilogue thread
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+    static constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
+};
+
+struct TileInfo {
+    int e, nt, row0, rows;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(int tile, const int* s_tiles, const int* s_off, const int* s_cnt,
+                                                int E) {
+    int lo = 0, hi = E;  // s_tiles[lo] <= tile < s_tiles[hi]
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (s_tiles[mid] <= tile)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    TileInfo ti;
+    ti.e = lo;
+    const int local = tile - s_tiles[lo];
+    const int mtc = (s_cnt[lo] + 127) >> 7;
+    ti.nt = local / mtc;
+    const int mt = local - ti.nt * mtc;
+    ti.row0 = s_off[lo] + mt * 128;
+    ti.rows = min(128, s_cnt[lo] - mt * 128);
+    return ti;
+}
+
+template <bool GATED>
+__global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmParams p) {
+    using C = GemmCfg<GATED>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+
+    __shared__ __align__(8) uint64_t full_bar[C::STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
+    __shared__ __align__(8) uint64_t tfull_bar[C::NBUF];
+    __shared__ __align__(8) uint64_t tempty_bar[C::NBUF];
+    __shared__ __align__(8) uint64_t drain_bar;
+    __shared__ __align__(8) uint64_t amax_bar;  // gate/up epilogue: the two column halves of a row meet here
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    __shared__ int s_tiles[kMaxExperts + 1], s_off[kMaxExperts + 1], s_cnt[kMaxExperts];
+    __shared__ float s_amax[2][2][128];  // [tile parity][column half][row]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int E = p.E;
+    for (int i = tid; i <= E; i += C::THREADS) {
+        s_tiles[i] = p.tiles[i];
+        s_off[i] = p.offset[i];
+        if (i < E) s_cnt[i] = p.count[i];
+    }
+    if (tid == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int b = 0; b < C::NBUF; ++b) {
+            mbar_init(smem_u32(&tfull_bar[b]), 1);
+            mbar_init(smem_u32(&tempty_bar[b]), C::EPI_WARPS);
+        }
+        mbar_init(smem_u32(&drain_bar), 1);
+        mbar_init(smem_u32(&amax_bar), C::EPI_WARPS * 32);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_slot;
+    const int total = s_tiles[E];
+    volatile int* abort_p = &abort_flag;
+    uint32_t* err = p.status + kStatusError;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t filled = 0;  // bit s: stage s was filled at least once
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const TileInfo ti = decode_tile(tile, s_tiles, s_off, s_cnt, E);
+                const int brow = ti.e * p.rows_B + ti.nt * 128;
+                for (int kb = 0; kb < p.KB; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full_bar[stage]);
+                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    const uint32_t a_dst = smem_u32(smem + stage * C::STAGE_BYTES);
+                    const uint32_t b_dst = a_dst + C::A_BYTES;
+                    tma_load_2d(a_dst, &tmA, kb * 128, ti.row0, fb);
+                    tma_load_2d(b_dst, &tmB, kb * 128, brow, fb);
+                    if (GATED) tma_load_2d(b_dst + 128 * 128, &tmB, kb * 128, brow + p.up_rows, fb);
+                    filled |= 1u << stage;
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Drain: the last fill of every stage has landed (TMA completion
+            // does not depend on the other roles) ...
+            int dummy = 0;
+            for (int i = 0; i < C::STAGES; ++i) {
+                int s = (stage + C::STAGES - 1 - i) % C::STAGES;
+                uint32_t ph = (s < stage) ? phase : phase ^ 1u;  // parity of that stage's last fill
+                if (filled & (1u << s)) mbar_wait(smem_u32(&full_bar[s]), ph, &dummy, err, kErrTimeoutProducer);
+            }
+            // ... and, on the normal path, every stage was released by the MMA
+            // commit, so no asynchronous arrive can land after this CTA exits.
+            if (ok) {
+                for (int i = 0; i < C::STAGES; ++i) {
+                    if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) break;
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------- MMA issuer
+            int stage = 0, buf = 0;
+            uint32_t sphase = 0, tphase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                for (int kb = 0; kb < p.KB; ++kb) {
+                    if (!mbar_wait(smem_u32(&full_bar[stage]), sphase, abort_p, err, kErrTimeoutMma) ||
+                        !mbar_wait(smem_u32(&tempty_bar[buf]), tphase ^ 1u, abort_p, err, kErrTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(smem + stage * C::STAGE_BYTES);
+                    const uint32_t b_base = a_base + C::A_BYTES;
+                    const uint32_t d = tmem_base + (uint32_t)(buf * C::BN);
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4)
+                        mma_e4m3(d, smem_desc_sw128(a_base + 32 * k4), smem_desc_sw128(b_base + 32 * k4), C::IDESC,
+                                 k4 > 0 ? 1u : 0u);
+                    mma_commit(smem_u32(&empty_bar[stage]));
+                    mma_commit(smem_u32(&tfull_bar[buf]));
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        sphase ^= 1u;
+                    }
+                    if (++buf == C::NBUF) {
+                        buf = 0;
+                        tphase ^= 1u;
+                    }
+                }
+            }
+            // every MMA issued above has completed before TMEM is released
+            mma_commit(smem_u32(&drain_bar));
+            int dummy = 0;
+            mbar_wait(smem_u32(&drain_bar), 0, &dummy, err, kErrTimeoutMma);
+        }
+    } else {
+        // -------------------------------------------- promotion + epilogue
+        const int ew = warp - 2;
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int half = ew >> 2;      // which half of the columns
+        const int row = quarter * 32 + lane;
+        const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
+        int buf = 0;
+        uint32_t tphase = 0;
+        uint32_t tpar = 0;  // parity of the tiles this CTA has finished
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, tpar ^= 1u) {
+            const TileInfo ti = decode_tile(tile, s_tiles, s_off, s_cnt, E);
+            const int grow = ti.row0 + row;
+            const bool valid = row < ti.rows;
+            const int grow_c = min(grow, p.R - 1);
+            float acc[C::COLS];
+            const uint16_t* bias_e = p.bias + (size_t)ti.e * (GATED ? 2 * p.N_real : p.N_real);
+            const int n0 = ti.nt * 128 + 64 * half;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const int n = n0 + i;
+                acc[i] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + n)) : 0.f;
+                if (GATED) acc[64 + i] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + p.N_real + n)) : 0.f;
+            }
+            const float* sa_row = p.sa + (size_t)grow_c * p.KB;
+            const float* sw_g = p.sw + ((size_t)ti.e * p.sw_rowblocks + ti.nt) * p.KB;
+            const float* sw_u = GATED ? p.sw + ((size_t)ti.e * p.sw_rowblocks + p.up_rows / 128 + ti.nt) * p.KB : sw_g;
+            for (int kb = 0; kb < p.KB; ++kb) {
+                const float a_s = __ldg(sa_row + kb);
+                const float fg = a_s * __ldg(sw_g + kb);
+                const float fu = GATED ? a_s * __ldg(sw_u + kb) : 0.f;
+                if (!mbar_wait(smem_u32(&tfull_bar[buf]), tphase, abort_p, err, kErrTimeoutEpilogue)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tcol = t_lane + (uint32_t)(buf * C::BN);
+                uint32_t r[32];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    tmem_ld32(tcol + 64 * half + 32 * c, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[32 * c + i] = fmaf(__uint_as_float(r[i]), fg, acc[32 * c + i]);
+                }
+                if (GATED) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        tmem_ld32(tcol + 128 + 64 * half + 32 * c, r);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            acc[64 + 32 * c + i] = fmaf(__uint_as_float(r[i]), fu, acc[64 + 32 * c + i]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[buf]));
+                if (++buf == C::NBUF) {
+                    buf = 0;
+                    tphase ^= 1u;
+                }
+            }
+            if (!ok) break;
+
+            if (GATED) {
+                // h = silu(g) * u for this thread's 64 columns of the 128-wide group
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    const float g = acc[i], u = acc[64 + i];
+                    const float h = (n0 + i < p.N_real) ? __fdividef(g, 1.0f + __expf(-g)) * u : 0.f;
+                    acc[i] = h;
+                    amax = fmaxf(amax, fabsf(h));
+                }
+                // the row's other 64 columns belong to the partner warp (same TMEM
+                // lane quarter); exchange the partial maxima through shared memory,
+                // double-buffered by tile parity, behind a bounded barrier
+                s_amax[tpar][half][row] = amax;
+                mbar_arrive(smem_u32(&amax_bar));
+                if (!mbar_wait(smem_u32(&amax_bar), tpar, abort_p, err, kErrTimeoutEpilogue)) break;
+                amax = fmaxf(s_amax[tpar][0][row], s_amax[tpar][1][row]);
+                const float s = group_scale(amax);
+                if (valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.hq + (size_t)grow * p.ldq + ti.nt * 128 + 64 * half);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int i = 16 * v + 4 * q;
+                            w[q] = quant4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3], s);
+                        }
+                        dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    if (half == 0) p.sh[(size_t)grow * (p.ldq / 128) + ti.nt] = s;
+                }
+            } else {
+                if (valid) {
+                    const int slot = __ldg(p.perm + grow);
+                    const float w = bf16_bits_to_f32(__ldg(p.topk_wb + slot));
+                    float4* dst = reinterpret_cast<float4*>(p.part + (size_t)slot * p.ldp + n0);
+#pragma unroll
+                    for (int v = 0; v < 16; ++v)
+                        dst[v] = make_float4(w * acc[4 * v], w * acc[4 * v + 1], w * acc[4 * v + 2], w * acc[4 * v + 3]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+template <bool GATED>
+static cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+                               cudaStream_t st) {
+    using C = GemmCfg<GATED>;
+    cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    moe_gemm_kernel<GATED><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_gateup(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+                               cudaStream_t st) {
+    return launch_gemm<true>(tmA, tmB, p, grid, st);
+}
+
+cudaError_t launch_gemm_down(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+                             cudaStream_t st) {
+    return launch_gemm<false>(tmA, tmB, p, grid, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,78 @@
+// Host-side launch wrappers and parameter blocks shared by the library's
+// translation units (not part of the public C ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+struct RouteParams {
+    const uint16_t* x;   // bf16 [T, H]
+    const uint16_t* rw;  // bf16 [E, H]
+    const uint16_t* rb;  // bf16 [E]
+    int T, H, E, k;
+    int nchunks;  // ceil(T / kChunkTokens)
+    int nt1, nt2; // n-tiles per 128-row M tile: gate/up GEMM (Ip/128), down GEMM (Hp/128)
+    int32_t* topk_idx;
+    float* topk_w;
+    uint16_t* topk_wb;
+    int32_t* hist;   // [nchunks, E], zeroed before the launch
+    int32_t* done;   // arrival counter, zeroed before the launch
+    int32_t* count;
+    int32_t* offset;
+    int32_t* chunk_base;
+    int32_t* tiles1;
+    int32_t* tiles2;
+    uint32_t* status;
+};
+
+struct PermuteParams {
+    const uint16_t* x;
+    int T, H, Hp, E, k;
+    int tokens_per_cta;
+    const int32_t* topk_idx;
+    const int32_t* chunk_base;
+    int32_t* perm;
+    int32_t* inv;
+    uint8_t* xq;  // [R, Hp]
+    float* sx;    // [R, Hp/128]
+};
+
+struct GemmParams {
+    int E, R, KB;          // K / 128
+    int N_real;            // gate/up GEMM: I; down GEMM: H
+    int rows_B;            // rows of one expert's weight matrix: 2*Ip or Hp
+    int up_rows;           // gate/up GEMM: Ip (row offset of the up half)
+    int sw_rowblocks;      // rows_B / 128
+    const int32_t* count;
+    const int32_t* offset;
+    const int32_t* tiles;  // [E+1] first tile of each expert
+    const float* sa;       // activation scales [R, KB]
+    const float* sw;       // weight scales [E, rows_B/128, KB]
+    const uint16_t* bias;  // gate/up: b13 [E, 2I]; down: b2 [E, H]
+    uint8_t* hq;           // gate/up output codes [R, ldq]
+    float* sh;             // gate/up output scales [R, ldq/128]
+    int ldq;
+    const int32_t* perm;      // down: row -> t*k + j
+    const uint16_t* topk_wb;  // down: routing weights bf16 [T*k]
+    float* part;              // down: [T*k, ldp]
+    int ldp;
+    uint32_t* status;
+};
+
+cudaError_t launch_router(const RouteParams& p, cudaStream_t st);
+cudaError_t launch_permute_quant(const PermuteParams& p, cudaStream_t st);
+cudaError_t launch_combine(const float* part, int T, int H, int ldp, int k, uint16_t* out, int num_sms,
+                           cudaStream_t st);
+cudaError_t launch_pack_blocks(const float* src, int E, int rows_src, int cols, int rows_p, int cols_p, int gated_I,
+                               uint8_t* q, float* s, cudaStream_t st);
+cudaError_t launch_quantize_rows(const float* in, int rows, int cols, int ld_in, uint8_t* q, float* s,
+                                 cudaStream_t st);
+cudaError_t launch_bounded_wait_test(uint64_t timeout_ns, int arrivals, uint32_t* result, cudaStream_t st);
+cudaError_t launch_gemm_gateup(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+                               cudaStream_t st);
+cudaError_t launch_gemm_down(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+                             cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,167 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle, on the GPU.
+
+Bit-exact: router indices, the permutation (counts, offsets, rows), the FP8
+codes and scales of x, the packed weights and the stand-alone quantiser.
+Within tolerance: routing weights (one bf16 step), requantised h (>= 99.9 %
+identical codes, the rest neighbours) and the bf16 output
+(max|d| <= 2e-2 max|oracle|, mean|d| <= 2e-3 mean|oracle|).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from harness import Layer, bf16_bits, check_codes_close, check_output, sample_tokens, torch_bf16_to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import sparse_moe_layer_gb300 as m
+    m.build()
+    assert torch.cuda.is_available()
+    return m
+
+
+def margin_safe_x(cfg, rw, rb, x=None):
+    """Draw x for an ad-hoc layer shape, redrawing rows whose top-k margin is below 1e-3."""
+    att = np.zeros(cfg.T, np.uint32)
+    x = synth.x_rows(cfg, att) if x is None else x
+    rows = np.arange(cfg.T)
+    while len(rows):
+        m = oracle.router(np.ascontiguousarray(x[rows]), rw, rb, cfg.top_k)["margin"]
+        rows = rows[m < 1e-3]
+        att[rows] += 1
+        if len(rows):
+            x[rows] = synth.x_rows(cfg, att, rows=rows)
+    return x
+
+
+def full_check(moe, layer: Layer, n_sample: int | None = None):
+    T, k, E = layer.T, layer.k, layer.E
+    layer.to_device()
+    out, v, ws = layer.run_gpu()
+    assert moe.read_device_status(ws) == 0
+    r = layer.oracle_router()
+    # routing: bit-exact indices, weights within one bf16 step
+    assert np.array_equal(v["topk_idx"].cpu().numpy(), r["idx"])
+    assert np.allclose(v["topk_w"].cpu().numpy(), r["w_f32"], rtol=2e-6, atol=1e-7)
+    wb_gpu = v["topk_wb"].cpu().view(torch.int16).numpy().view(np.uint16).astype(np.int32)
+    assert np.all(np.abs(wb_gpu - r["w_bf16"].astype(np.int32)) <= 1)
+    # grouping by expert: bit-exact
+    p = oracle.permute(r["idx"], E)
+    for key in ("count", "offset", "perm", "inv"):
+        assert np.array_equal(v[key].cpu().numpy(), p[key]), key
+    # GEMM tile lists cover every expert's rows
+    mt = (p["count"] + 127) // 128
+    st = v["status"].cpu().numpy()
+    assert st[1] == mt.sum() * (layer.Ip // 128) and st[2] == mt.sum() * (layer.Hp // 128)
+    # x quantisation: bit-exact codes and scales in every permuted row
+    xq, sx = oracle.quant_rows_bf16(layer.x)
+    tok_of_row = p["perm"] // k
+    assert np.array_equal(v["xq"].cpu().numpy(), xq[tok_of_row])
+    assert np.array_equal(v["sx"].cpu().numpy(), sx[tok_of_row])
+    # layer output (all tokens, or a sample including the most/least loaded experts)
+    tokens = np.arange(T, dtype=np.int32) if n_sample is None else sample_tokens(r["idx"], E, n_sample)
+    o_out, inter = layer.oracle_forward(tokens, r["idx"])
+    rel = check_output(torch_bf16_to_np(out)[tokens], o_out)
+    # requantised h of the same (token, slot) rows
+    rows = p["inv"][(tokens[:, None] * k + np.arange(k)[None, :]).ravel()]
+    frac = check_codes_close(v["hq"].cpu().numpy()[rows], inter["hq"])
+    assert np.allclose(v["sh"].cpu().numpy()[rows], inter["sh"], rtol=2e-3, atol=0)
+    return out, rel, frac
+
+
+def test_bounded_wait_returns_instead_of_hanging(moe):
+    assert moe.test_bounded_wait(10 ** 9, 1) == 1
+    assert moe.test_bounded_wait(2 * 10 ** 6, 0) == 2  # nothing arrives: gives up after 2 ms
+
+
+def test_quantize_rows_bit_exact(moe):
+    rng = np.random.default_rng(7)
+    v = (rng.standard_normal((33, 300)) * np.exp(rng.uniform(-8, 8, (33, 1)))).astype(np.float32)
+    v[3] = 0.0
+    v[5, 128:256] = 0.0
+    v[6, :7] = np.float32([448.0, -448.0, 1e-30, -1e-30, 2.0 ** -9, 3.0, -0.0])
+    q, s = moe.quantize_rows(torch.from_numpy(v).cuda())
+    qo, so = oracle.quant_rows_f32(v)
+    assert np.array_equal(q.cpu().numpy(), qo)
+    assert np.array_equal(s.cpu().numpy(), so)
+
+
+@pytest.mark.parametrize("H,I,E", [(256, 256, 2), (200, 130, 3), (2880, 2880, 1)])
+def test_pack_weights_bit_exact(moe, H, I, E):
+    rng = np.random.default_rng(H + I)
+    w13 = (rng.standard_normal((E, 2 * I, H)) * 0.02).astype(np.float32)
+    w2 = (rng.standard_normal((E, H, I)) * 0.02).astype(np.float32)
+    w13[0, :128, :128] = 0.0  # an all-zero block
+    q13, s13, q2, s2 = moe.pack_weights(torch.from_numpy(w13).cuda(), torch.from_numpy(w2).cuda())
+    oq13, os13 = oracle.pack_w13(w13)
+    oq2, os2 = oracle.pack_w2(w2)
+    assert np.array_equal(q13.cpu().numpy(), oq13) and np.array_equal(s13.cpu().numpy(), os13)
+    assert np.array_equal(q2.cpu().numpy(), oq2) and np.array_equal(s2.cpu().numpy(), os2)
+
+
+def test_tiny_layer_all_tokens(moe):
+    out, rel, frac = full_check(moe, Layer(synth.config("tiny")))
+    assert rel[0] < 2e-2
+
+
+def _adhoc(name, T, H, I, E, k, seed=11, rb=None, rw_zero=False):
+    """An ad-hoc layer shape from the generator; rb (float) overrides the router bias."""
+    cfg = synth.LayerConfig(name, T, H, I, E, k, seed, "normal", "normal")
+    rw, rb_gen = synth.router(cfg)
+    if rw_zero:
+        rw = np.zeros_like(rw)
+    rb = rb_gen if rb is None else bf16_bits(np.asarray(rb, np.float32))
+    x = synth.x_rows(cfg) if rw_zero else margin_safe_x(cfg, rw, rb)
+    return Layer(cfg, x=x, rw=rw, rb=rb)
+
+
+def test_single_token(moe):
+    full_check(moe, _adhoc("one_token", 1, 256, 256, 8, 2))
+
+
+def test_ragged_hidden_and_intermediate(moe):
+    full_check(moe, _adhoc("ragged", 37, 200, 136, 5, 3))
+
+
+def test_all_tokens_to_two_experts_multi_tile(moe):
+    # experts 0 and 1 get every token (3 M tiles each: 128 + 128 + 44 rows); experts 2..7 get none
+    rb = np.array([8.0, 8.0, 0, 0, 0, 0, 0, 0], np.float32)
+    layer = _adhoc("skewed", 300, 256, 256, 8, 2, rb=rb)
+    full_check(moe, layer)
+
+
+def test_top_k_equals_E(moe):
+    full_check(moe, _adhoc("k_eq_E", 20, 256, 384, 4, 4))
+
+
+def test_equal_logits_pick_lowest_experts(moe):
+    layer = _adhoc("ties", 16, 256, 256, 8, 3, rb=np.zeros(8, np.float32), rw_zero=True)
+    layer.to_device()
+    _, v, _ = layer.run_gpu()
+    assert np.all(v["topk_idx"].cpu().numpy() == [0, 1, 2])
+    w = v["topk_w"].cpu().numpy()
+    assert np.allclose(w, 1.0 / 3.0, rtol=1e-6)
+
+
+def test_many_tokens_uses_blocked_router_and_permute(moe):
+    # T > 2048 switches the router to 4 tokens per CTA and the permutation to 8 tokens per CTA
+    full_check(moe, _adhoc("many_tokens", 2500, 256, 256, 8, 2), n_sample=48)
+
+
+def test_repeated_calls_are_bit_identical(moe):
+    layer = Layer(synth.config("tiny")).to_device()
+    a, _, ws = layer.run_gpu()
+    b, _, _ = layer.run_gpu(workspace=ws)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("name,n_sample", [("oss20b_decode", None), ("oss120b_decode", 32),
+                                           ("oss120b_prefill", 24), ("qwen235b_prefill", 24)])
+def test_layer_shapes_full_size(moe, name, n_sample):
+    full_check(moe, Layer(synth.config(name)), n_sample=n_sample)
+    torch.cuda.empty_cache()
