@@ -1,0 +1,403 @@
+#!/usr/bin/env python
+"""MoE-layer tokens/s on one GB300 (sparse gpt-oss-style MoE MLP forward).
+
+One step = one call of the whole layer (router, top-k + softmax, grouping by
+expert + FP8 quantisation of x, gate/up GEMM + SwiGLU + requant, down GEMM +
+routing-weight scale, combine) over one batch of T synthetic tokens whose
+inputs are resident in HBM.  L2 is flushed (256 MiB write) before every step
+and the step is timed with CUDA events on the launching stream; the flush is
+outside the events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Multi-GPU: one process per GPU (torchrun), each an independent replica of the
+same workload (the layer has no exchange step on one GPU): weak scaling,
+value = tokens of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s on 1 GB300; % of HBM (decode) / FP8 TC peak (prefill)"
+DEFAULT_CONFIG = "oss20b_decode"
+FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]), bf16_sust=float(p["bf16_tflops_sustained"]),
+                    source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, source="fallback")
+
+
+def workload_str(cfg) -> str:
+    return (f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top_k={cfg.top_k} seed={cfg.seed} "
+            f"router_b={cfg.router_b} expert_bias={cfg.expert_bias}")
+
+
+def algorithmic(cfg, counts: np.ndarray) -> dict:
+    """Algorithmic bytes / FLOPs (unpadded; activated experts only)."""
+    H, I, T, k, E = cfg.H, cfg.I, cfg.T, cfg.top_k, cfg.E
+    R = T * k
+    act = int((counts > 0).sum())
+    hb, ib = -(-H // 128), -(-I // 128)
+    w13 = act * (2 * I * H + 4 * 2 * ib * hb + 2 * 2 * I)
+    w2 = act * (H * I + 4 * hb * ib + 2 * H)
+    gemm1_bytes = w13 + R * H + 4 * R * hb + R * I + 4 * R * ib
+    gemm2_bytes = w2 + R * I + 4 * R * ib + 4 * R * H
+    step_bytes = w13 + w2 + E * H * 2 + E * 2 + T * H * 2 + T * H * 2
+    return dict(active=act, gemm1_bytes=gemm1_bytes, gemm2_bytes=gemm2_bytes, step_bytes=step_bytes,
+                gemm1_flops=2 * R * 2 * I * H, gemm2_flops=2 * R * H * I, router_flops=2 * T * E * H)
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for f in ("moe_gemm.cu", "moe_device.cuh"):
+        with open(os.path.join(ROOT, "sparse_moe_layer_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, cfg_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            t = json.load(f)
+        rec = t.get(f"{kernel}@{cfg_name}")
+        if rec and rec.get("source_digest") == source_digest():
+            return int(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms in a child process."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid: str | None):
+        self.proc = None
+        self.lines = []
+        sel = [f"--id={gpu_uuid}"] if gpu_uuid else []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", *sel, f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l.strip() for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return dict(sm_mhz=None, sm_max_mhz=mx, reasons=sorted(reasons), samples=0)
+        loaded = [s for s in sm if s > 0.5 * (mx or max(sm))] or sm
+        return dict(sm_mhz=statistics.median(loaded), sm_max_mhz=mx, reasons=sorted(reasons), samples=len(sm))
+
+
+def build_layer(cfg, device):
+    """Inputs of the workload resident on the device; weights packed by the library."""
+    import torch
+    import sparse_moe_layer_gb300 as moe
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    x = synth.layer_x(cfg)
+    rw, rb = synth.router(cfg)
+    b13, b2 = synth.expert_biases(cfg)
+    E, H, I, Hp, Ip = cfg.E, cfg.H, cfg.I, cfg.Hp, cfg.Ip
+    w13 = torch.empty((E, 2 * Ip, Hp), dtype=torch.uint8, device=device)
+    s13 = torch.empty((E, 2 * Ip // 128, Hp // 128), dtype=torch.float32, device=device)
+    w2 = torch.empty((E, Hp, Ip), dtype=torch.uint8, device=device)
+    s2 = torch.empty((E, Hp // 128, Ip // 128), dtype=torch.float32, device=device)
+    chunk = 8
+    for e0 in range(0, E, chunk):
+        n = min(chunk, E - e0)
+        m13 = torch.from_numpy(synth.w13_master(cfg, e0, n)).to(device)
+        m2 = torch.from_numpy(synth.w2_master(cfg, e0, n)).to(device)
+        moe.pack_weights_into(m13, m2, H, I, n, w13[e0:e0 + n], s13[e0:e0 + n], w2[e0:e0 + n], s2[e0:e0 + n])
+        torch.cuda.synchronize()
+        del m13, m2
+    layer = moe.MoeLayer(bf16(rw), bf16(rb), w13, s13, bf16(b13), w2, s2, bf16(b2), cfg.top_k)
+    return layer, bf16(x), x
+
+
+def cpu_oracle_leg(cfg, n_units: int, steps: int = 1):
+    """Time the oracle (single thread) on a bounded sample of the workload.
+
+    A unit is one (token, slot) expert evaluation: 1/top_k of a token.  Returns
+    (tokens per second, sample description, seconds)."""
+    import oracle
+    x = synth.layer_x(cfg)
+    rw, rb = synth.router(cfg)
+    b13, b2 = synth.expert_biases(cfg)
+    k = cfg.top_k
+    n_tok = max(1, -(-n_units // k))
+    rng = np.random.default_rng(1234)
+    tokens = np.sort(rng.choice(cfg.T, size=min(n_tok, cfg.T), replace=False)).astype(np.int32)
+    r = oracle.router(np.ascontiguousarray(x[tokens]), rw, rb, k)
+    needed = np.unique(r["idx"])
+    E, Hp, Ip = cfg.E, cfg.Hp, cfg.Ip
+    q13 = np.zeros((E, 2 * Ip, Hp), np.uint8)
+    s13 = np.ones((E, 2 * Ip // 128, Hp // 128), np.float32)
+    q2 = np.zeros((E, Hp, Ip), np.uint8)
+    s2 = np.ones((E, Hp // 128, Ip // 128), np.float32)
+    from concurrent.futures import ThreadPoolExecutor
+
+    def pack(e):  # weight conversion is offline for both sides: untimed
+        oracle.pack_w13(synth.w13_master(cfg, int(e), 1), q13[e:e + 1], s13[e:e + 1])
+        oracle.pack_w2(synth.w2_master(cfg, int(e), 1), q2[e:e + 1], s2[e:e + 1])
+
+    with ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
+        list(ex.map(pack, needed))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.forward(x, rw, rb, q13, s13, b13, q2, s2, b2, k, tokens=tokens)
+    dt = time.perf_counter() - t0
+    return steps * len(tokens) / dt, f"{len(tokens)} of {cfg.T} tokens ({len(needed)} experts), full layer per token", dt
+
+
+def run_reference(args, cfg, rank):
+    """The oracle as the reference arm: K steps, each a bounded sample (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    x = synth.layer_x(cfg)
+    rw, rb = synth.router(cfg)
+    b13, b2 = synth.expert_biases(cfg)
+    k = cfg.top_k
+    rng = np.random.default_rng(99)
+    tokens_all = rng.permutation(cfg.T).astype(np.int32)
+    r = oracle.router(np.ascontiguousarray(x[tokens_all]), rw, rb, k)
+    E, Hp, Ip = cfg.E, cfg.Hp, cfg.Ip
+    q13 = np.zeros((E, 2 * Ip, Hp), np.uint8)
+    s13 = np.ones((E, 2 * Ip // 128, Hp // 128), np.float32)
+    q2 = np.zeros((E, Hp, Ip), np.uint8)
+    s2 = np.ones((E, Hp // 128, Ip // 128), np.float32)
+    from concurrent.futures import ThreadPoolExecutor
+    needed = np.unique(r["idx"])
+
+    def pack(e):
+        oracle.pack_w13(synth.w13_master(cfg, int(e), 1), q13[e:e + 1], s13[e:e + 1])
+        oracle.pack_w2(synth.w2_master(cfg, int(e), 1), q2[e:e + 1], s2[e:e + 1])
+
+    with ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
+        list(ex.map(pack, needed))
+    # one token per step, cycling through a seeded permutation of the batch
+    def step(i):
+        t = tokens_all[i % len(tokens_all)]
+        oracle.forward(x, rw, rb, q13, s13, b13, q2, s2, b2, k, tokens=np.array([t], np.int32))
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    line = dict(metric=METRIC, value=value, unit="tokens/s", n_gpus=args.gpus, steps=args.steps, warmup=args.warmup,
+                ms_per_step=dt * 1e3 / args.steps, higher_is_better=True, scaling="weak", vs_baseline=None,
+                dtype="f64", data="synthetic", impl="reference",
+                config=dict(workload=workload_str(cfg), step="one token of the batch through the whole layer"),
+                cpu_baseline=dict(value=value, unit="tokens/s", cores=1, kind="oracle",
+                                  sample=f"{args.steps} tokens, one per step, single-threaded fp64 C oracle"),
+                e2e=dict(value=value, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=[c.name for c in synth.CONFIGS])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-units", type=int, default=32, help="(token, slot) units in the CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    cfg = synth.config(args.config)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, cfg, rank)
+        return
+
+    import torch
+    import sparse_moe_layer_gb300 as moe
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    layer, x_dev, x_host_np = build_layer(cfg, dev)
+    T, H = cfg.T, cfg.H
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        layer(x_dev, out=out)
+    torch.cuda.synchronize()
+    ws = layer.workspace(T)
+    assert moe.read_device_status(ws) == 0, "device wait timed out during warm-up"
+    counts = moe.workspace_views(ws, T, cfg.H, cfg.I, cfg.E, cfg.top_k)["count"].cpu().numpy()
+    alg = algorithmic(cfg, counts)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for row in ev:  # torch creates the CUDA event on first record
+        for e in row:
+            e.record(stream)
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    time.sleep(0.25)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        moe.forward(x_dev, layer.router_w, layer.router_b, layer.w13, layer.s13, layer.b13, layer.w2, layer.s2,
+                    layer.b2, cfg.top_k, out=out, workspace=ws, events=ev[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if pg:
+        pg.barrier()
+    sampler.stop()
+    status = moe.read_device_status(ws)
+    step_ms = [ev[i][0].elapsed_time(ev[i][5]) for i in range(K)]
+    stage_ms = {s: statistics.fmean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
+                for j, s in enumerate(moe.STAGES)}
+    ms = statistics.fmean(step_ms)
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the public API with host buffers: H2D of x, the layer, D2H of out
+    x_host = torch.from_numpy(np.ascontiguousarray(x_host_np).view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_stage = torch.empty_like(x_dev)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(min(args.warmup, 5)):
+        x_stage.copy_(x_host, non_blocking=True)
+        layer(x_stage, out=out)
+        out_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        e2e_ev[i][0].record(stream)
+        x_stage.copy_(x_host, non_blocking=True)
+        layer(x_stage, out=out)
+        out_host.copy_(out, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.fmean(a.elapsed_time(b) for a, b in e2e_ev)
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert torch.equal(out_host.view(torch.int16), out.cpu().view(torch.int16))
+
+    pk = peaks()
+    prefill = cfg.T >= 2048
+    g1_s = stage_ms["gemm_gateup"] * 1e-3
+    if prefill:
+        fp8_peak = 2.0 * pk["bf16"]  # FP8 dense = 2 x bf16 dense (nominal ratio)
+        roof = dict(bound="tensor", achieved=alg["gemm1_flops"] / g1_s / 1e12, peak=fp8_peak, unit="TFLOP/s")
+    else:
+        roof = dict(bound="hbm", achieved=alg["gemm1_bytes"] / g1_s / 1e9, peak=pk["hbm"], unit="GB/s")
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = recorded_traffic("gemm_gateup", cfg.name)
+    roof["kernel"] = "moe_gemm_kernel<true> (gate/up GEMM + SwiGLU + requant)"
+    roof["peak_source"] = pk["source"] + (" (hbm_gbs)" if not prefill else " (2 x bf16_tflops burst)")
+    roof["algorithmic_per_launch"] = alg["gemm1_bytes"] if not prefill else alg["gemm1_flops"]
+
+    value = world * T / (ms * 1e-3)
+    line = dict(metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=K, warmup=args.warmup,
+                ms_per_step=ms, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="e4m3",
+                data="synthetic",
+                config=dict(workload=workload_str(cfg), parallelism=f"replicas{world}",
+                            l2="flushed before every step (256 MiB write, outside the timed events)",
+                            weights="FP8 e4m3 128x128 block scales, packed on device by moe_pack_weights"),
+                roofline=roof,
+                step=dict(ms_per_stage=stage_ms, active_experts=alg["active"],
+                          step_GBps=alg["step_bytes"] / (ms * 1e-3) / 1e9,
+                          step_hbm_frac=alg["step_bytes"] / (ms * 1e-3) / 1e9 / pk["hbm"],
+                          gemm_tflops=(alg["gemm1_flops"] + alg["gemm2_flops"]) / (ms * 1e-3) / 1e12,
+                          wall_s=wall, device_status=status),
+                e2e=dict(value=world * T / (e2e_ms * 1e-3), unit="tokens/s", h2d_bytes_per_step=T * H * 2,
+                         d2h_bytes_per_step=T * H * 2, ms_per_step=e2e_ms),
+                gpu_launches=5 * K,
+                clocks=sampler.summary())
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, dt = cpu_oracle_leg(cfg, args.cpu_units)
+        line["cpu_baseline"] = dict(value=v, unit="tokens/s", cores=1, kind="oracle", sample=desc, seconds=dt)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -65,12 +65,13 @@ typedef enum {
 typedef struct {
     size_t total_bytes;
     size_t status;     /* uint32[64]: [0] device error word, [1] tile total GEMM1, [2] tile total GEMM2 */
-    size_t hist;       /* int32 [ceil(T/256), E] tokens per (256-token chunk, expert) + done counter */
+    size_t hist;       /* int32 [ceil(T/256), E] tokens per (256-token chunk, expert), then 1 + T arrival counters */
     size_t count;      /* int32 [E]     rows per expert */
     size_t offset;     /* int32 [E+1]   first row of each expert (exclusive scan of count) */
     size_t chunk_base; /* int32 [ceil(T/256), E] first row of each (chunk, expert) */
     size_t tiles1;     /* int32 [E+1]   first gate/up GEMM tile of each expert */
     size_t tiles2;     /* int32 [E+1]   first down GEMM tile of each expert */
+    size_t logits;     /* float [T, E] router logits (decode-sized batches only) */
     size_t topk_idx;   /* int32 [T, top_k] selected experts, ascending */
     size_t topk_w;     /* float [T, top_k] softmax weights before bf16 rounding */
     size_t topk_wb;    /* bf16  [T, top_k] routing weights used by the layer */
@@ -104,6 +105,17 @@ moe_status moe_get_workspace_layout(int T, int H, int I, int E, int top_k, moe_w
 moe_status moe_forward(const void* x, const void* router_w, const void* router_b, const uint8_t* w13, const float* s13,
                        const void* b13, const uint8_t* w2, const float* s2, const void* b2, int T, int H, int I, int E,
                        int top_k, void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * moe_forward with timing marks: events[0..5] are cudaEvent_t handles the
+ * caller created; events[i] is recorded on `stream` just before stage i
+ * (0 router, 1 permutation + x quantisation, 2 gate/up GEMM, 3 down GEMM,
+ * 4 combine) and events[5] after the last stage.  Same kernels, same results.
+ */
+moe_status moe_forward_profiled(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
+                                const float* s13, const void* b13, const uint8_t* w2, const float* s2, const void* b2,
+                                int T, int H, int I, int E, int top_k, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream, void* const* events);
 
 /*
  * Weight packer (the offline converter from master weights to the layer's

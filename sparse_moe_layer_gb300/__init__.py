@@ -28,7 +28,8 @@ class MoeError(RuntimeError):
         self.code = code
 
 
-_LAYOUT_FIELDS = ["total_bytes", "status", "hist", "count", "offset", "chunk_base", "tiles1", "tiles2", "topk_idx",
+_LAYOUT_FIELDS = ["total_bytes", "status", "hist", "count", "offset", "chunk_base", "tiles1", "tiles2", "logits",
+                  "topk_idx",
                   "topk_w", "topk_wb", "perm", "inv", "xq", "sx", "hq", "sh", "part"]
 
 
@@ -53,6 +54,8 @@ def lib():
         L.moe_get_workspace_layout.restype = i32
         L.moe_forward.argtypes = [vp] * 9 + [i32] * 5 + [vp, vp, sz, vp]
         L.moe_forward.restype = i32
+        L.moe_forward_profiled.argtypes = [vp] * 9 + [i32] * 5 + [vp, vp, sz, vp, vp]
+        L.moe_forward_profiled.restype = i32
         L.moe_pack_weights.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
         L.moe_pack_weights.restype = i32
         L.moe_quantize_rows.argtypes = [vp, i32, i32, i32, vp, vp, vp]
@@ -126,6 +129,7 @@ def workspace_views(ws: torch.Tensor, T: int, H: int, I: int, E: int, top_k: int
         chunk_base=v("chunk_base", nch * E, torch.int32, (nch, E)),
         tiles1=v("tiles1", E + 1, torch.int32, (E + 1,)),
         tiles2=v("tiles2", E + 1, torch.int32, (E + 1,)),
+        logits=v("logits", T * E, torch.float32, (T, E)),
         topk_idx=v("topk_idx", R, torch.int32, (T, top_k)),
         topk_w=v("topk_w", R, torch.float32, (T, top_k)),
         topk_wb=v("topk_wb", R, torch.bfloat16, (T, top_k)),
@@ -139,8 +143,15 @@ def workspace_views(ws: torch.Tensor, T: int, H: int, I: int, E: int, top_k: int
     )
 
 
-def forward(x, router_w, router_b, w13, s13, b13, w2, s2, b2, top_k: int, out=None, workspace=None, stream=None):
-    """out [T, H] bf16 = the MoE layer applied to x [T, H] bf16 (see moe_forward)."""
+STAGES = ("router", "permute_quant", "gemm_gateup", "gemm_down", "combine")
+
+
+def forward(x, router_w, router_b, w13, s13, b13, w2, s2, b2, top_k: int, out=None, workspace=None, stream=None,
+            events=None):
+    """out [T, H] bf16 = the MoE layer applied to x [T, H] bf16 (see moe_forward).
+
+    events: optional list of 6 torch.cuda.Event(enable_timing=True); event i is
+    recorded before stage i (STAGES) and event 5 after the last stage."""
     T, H = x.shape
     E = router_w.shape[0]
     I = b13.shape[1] // 2
@@ -157,8 +168,15 @@ def forward(x, router_w, router_b, w13, s13, b13, w2, s2, b2, top_k: int, out=No
             _dev(router_b, torch.bfloat16, "router_b"), _dev(w13, torch.uint8, "w13"), _dev(s13, torch.float32, "s13"),
             _dev(b13, torch.bfloat16, "b13"), _dev(w2, torch.uint8, "w2"), _dev(s2, torch.float32, "s2"),
             _dev(b2, torch.bfloat16, "b2")]
-    code = lib().moe_forward(*ptrs, T, H, I, E, top_k, _dev(out, torch.bfloat16, "out"),
-                             _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
+    tail = (_dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+            _stream(stream))
+    if events is None:
+        code = lib().moe_forward(*ptrs, T, H, I, E, top_k, *tail)
+    else:
+        if len(events) != 6:
+            raise ValueError("events must hold 6 CUDA events")
+        arr = (ctypes.c_void_p * 6)(*[ev.cuda_event for ev in events])
+        code = lib().moe_forward_profiled(*ptrs, T, H, I, E, top_k, *tail, arr)
     _check(code, "moe_forward")
     return out
 

@@ -40,12 +40,13 @@ void layout_of(int T, int H, int I, int E, int k, moe_workspace_layout* L) {
         return at;
     };
     L->status = take(kStatusWords * 4);
-    L->hist = take((nch * E + 1) * 4);  // + arrival counter
+    L->hist = take((nch * E + 1 + (size_t)T) * 4);  // + arrival counter + per-token counters
     L->count = take((size_t)E * 4);
     L->offset = take((size_t)(E + 1) * 4);
     L->chunk_base = take(nch * E * 4);
     L->tiles1 = take((size_t)(E + 1) * 4);
     L->tiles2 = take((size_t)(E + 1) * 4);
+    L->logits = take((size_t)T * E * 4);
     L->topk_idx = take(R * 4);
     L->topk_w = take(R * 4);
     L->topk_wb = take(R * 2);
@@ -99,6 +100,14 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 }  // namespace
 
+// Launch sequence shared by moe_forward and moe_forward_profiled; when `ev`
+// is non-null, ev[i] is recorded on the stream before stage i and ev[5]
+// after the last stage.
+static moe_status forward_impl(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
+                               const float* s13, const void* b13, const uint8_t* w2, const float* s2, const void* b2,
+                               int T, int H, int I, int E, int top_k, void* out, void* workspace,
+                               size_t workspace_bytes, void* stream, void* const* ev);
+
 extern "C" {
 
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k) {
@@ -117,6 +126,30 @@ moe_status moe_get_workspace_layout(int T, int H, int I, int E, int top_k, moe_w
 moe_status moe_forward(const void* x, const void* router_w, const void* router_b, const uint8_t* w13, const float* s13,
                        const void* b13, const uint8_t* w2, const float* s2, const void* b2, int T, int H, int I, int E,
                        int top_k, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    return forward_impl(x, router_w, router_b, w13, s13, b13, w2, s2, b2, T, H, I, E, top_k, out, workspace,
+                        workspace_bytes, stream, nullptr);
+}
+
+moe_status moe_forward_profiled(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
+                                const float* s13, const void* b13, const uint8_t* w2, const float* s2, const void* b2,
+                                int T, int H, int I, int E, int top_k, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream, void* const* events) {
+    if (!events) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 6; ++i)
+        if (!events[i]) return MOE_ERR_INVALID_ARG;
+    return forward_impl(x, router_w, router_b, w13, s13, b13, w2, s2, b2, T, H, I, E, top_k, out, workspace,
+                        workspace_bytes, stream, events);
+}
+
+}  // extern "C"
+
+static moe_status forward_impl(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
+                               const float* s13, const void* b13, const uint8_t* w2, const float* s2, const void* b2,
+                               int T, int H, int I, int E, int top_k, void* out, void* workspace,
+                               size_t workspace_bytes, void* stream, void* const* ev) {
+    auto mark = [&](int i) {
+        if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), static_cast<cudaStream_t>(stream));
+    };
     if (!x || !router_w || !router_b || !w13 || !s13 || !b13 || !w2 || !s2 || !b2 || !out || !workspace)
         return MOE_ERR_INVALID_ARG;
     if (!sizes_ok(T, H, I, E, top_k)) return MOE_ERR_INVALID_ARG;
@@ -135,6 +168,7 @@ moe_status moe_forward(const void* x, const void* router_w, const void* router_b
     const int sms = num_sms();
 
     // status words and the (chunk, expert) histogram start at zero
+    mark(0);
     if (cudaMemsetAsync(ws, 0, L.count, st) != cudaSuccess) return MOE_ERR_CUDA;
 
     RouteParams rp;
@@ -153,6 +187,8 @@ moe_status moe_forward(const void* x, const void* router_w, const void* router_b
     rp.topk_wb = reinterpret_cast<uint16_t*>(ws + L.topk_wb);
     rp.hist = reinterpret_cast<int32_t*>(ws + L.hist);
     rp.done = rp.hist + (size_t)nch * E;
+    rp.tok_cnt = rp.done + 1;
+    rp.logits = reinterpret_cast<float*>(ws + L.logits);
     rp.count = reinterpret_cast<int32_t*>(ws + L.count);
     rp.offset = reinterpret_cast<int32_t*>(ws + L.offset);
     rp.chunk_base = reinterpret_cast<int32_t*>(ws + L.chunk_base);
@@ -160,6 +196,7 @@ moe_status moe_forward(const void* x, const void* router_w, const void* router_b
     rp.tiles2 = reinterpret_cast<int32_t*>(ws + L.tiles2);
     rp.status = reinterpret_cast<uint32_t*>(ws + L.status);
     if (launch_router(rp, st) != cudaSuccess) return MOE_ERR_CUDA;
+    mark(1);
 
     PermuteParams pp;
     pp.x = rp.x;
@@ -176,6 +213,7 @@ moe_status moe_forward(const void* x, const void* router_w, const void* router_b
     pp.xq = ws + L.xq;
     pp.sx = reinterpret_cast<float*>(ws + L.sx);
     if (launch_permute_quant(pp, st) != cudaSuccess) return MOE_ERR_CUDA;
+    mark(2);
 
     // upper bound of the tile count of either GEMM: sum_e ceil(count_e/128) <= E + R/128
     const long long mt_bound = (long long)E + (R + 127) / 128;
@@ -207,6 +245,7 @@ moe_status moe_forward(const void* x, const void* router_w, const void* router_b
     long long t1 = mt_bound * (Ip / 128);
     int grid1 = (int)(t1 < sms ? t1 : sms);
     if (launch_gemm_gateup(tmA1, tmB1, g1, grid1, st) != cudaSuccess) return MOE_ERR_CUDA;
+    mark(3);
 
     GemmParams g2;
     memset(&g2, 0, sizeof(g2));
@@ -231,11 +270,15 @@ moe_status moe_forward(const void* x, const void* router_w, const void* router_b
     long long t2 = mt_bound * (Hp / 128);
     int grid2 = (int)(t2 < sms ? t2 : sms);
     if (launch_gemm_down(tmA2, tmB2, g2, grid2, st) != cudaSuccess) return MOE_ERR_CUDA;
+    mark(4);
 
     if (launch_combine(g2.part, T, H, Hp, top_k, static_cast<uint16_t*>(out), sms, st) != cudaSuccess)
         return MOE_ERR_CUDA;
+    mark(5);
     return MOE_OK;
 }
+
+extern "C" {
 
 moe_status moe_pack_weights(const float* w13_f32, const float* w2_f32, int H, int I, int E, uint8_t* w13, float* s13,
                             uint8_t* w2, float* s2, void* stream) {

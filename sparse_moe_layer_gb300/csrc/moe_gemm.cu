@@ -241,30 +241,54 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             const float* sa_row = p.sa + (size_t)grow_c * p.KB;
             const float* sw_g = p.sw + ((size_t)ti.e * p.sw_rowblocks + ti.nt) * p.KB;
             const float* sw_u = GATED ? p.sw + ((size_t)ti.e * p.sw_rowblocks + p.up_rows / 128 + ti.nt) * p.KB : sw_g;
+            // Warps whose TMEM lane quarter holds no valid row of this tile only
+            // keep the buffer hand-over going (decode tiles have few rows).
+            const bool active = quarter * 32 < ti.rows;
+            // scales of K blocks kb and kb+1 are in registers; kb+2 is loaded
+            // while kb is promoted, so no K block waits on a global load
+            float a0 = 0.f, g0 = 0.f, u0 = 0.f, a1 = 0.f, g1 = 0.f, u1 = 0.f;
+            if (active) {
+                a0 = __ldg(sa_row);
+                g0 = __ldg(sw_g);
+                if (GATED) u0 = __ldg(sw_u);
+                if (p.KB > 1) {
+                    a1 = __ldg(sa_row + 1);
+                    g1 = __ldg(sw_g + 1);
+                    if (GATED) u1 = __ldg(sw_u + 1);
+                }
+            }
             for (int kb = 0; kb < p.KB; ++kb) {
-                const float a_s = __ldg(sa_row + kb);
-                const float fg = a_s * __ldg(sw_g + kb);
-                const float fu = GATED ? a_s * __ldg(sw_u + kb) : 0.f;
+                float a2 = 0.f, g2 = 0.f, u2 = 0.f;
+                if (active && kb + 2 < p.KB) {
+                    a2 = __ldg(sa_row + kb + 2);
+                    g2 = __ldg(sw_g + kb + 2);
+                    if (GATED) u2 = __ldg(sw_u + kb + 2);
+                }
                 if (!mbar_wait(smem_u32(&tfull_bar[buf]), tphase, abort_p, err, kErrTimeoutEpilogue)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t tcol = t_lane + (uint32_t)(buf * C::BN);
-                uint32_t r[32];
+                if (active) {
+                    const float fg = a0 * g0;
+                    const uint32_t tcol = t_lane + (uint32_t)(buf * C::BN);
+                    uint32_t r[16];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    tmem_ld32(tcol + 64 * half + 32 * c, r);
+                    for (int c = 0; c < 4; ++c) {
+                        tmem_ld16(tcol + 64 * half + 16 * c, r);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[32 * c + i] = fmaf(__uint_as_float(r[i]), fg, acc[32 * c + i]);
-                }
-                if (GATED) {
+                        for (int i = 0; i < 16; ++i)
+                            acc[16 * c + i] = fmaf(__uint_as_float(r[i]), fg, acc[16 * c + i]);
+                    }
+                    if (GATED) {
+                        const float fu = a0 * u0;
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        tmem_ld32(tcol + 128 + 64 * half + 32 * c, r);
+                        for (int c = 0; c < 4; ++c) {
+                            tmem_ld16(tcol + 128 + 64 * half + 16 * c, r);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            acc[64 + 32 * c + i] = fmaf(__uint_as_float(r[i]), fu, acc[64 + 32 * c + i]);
+                            for (int i = 0; i < 16; ++i)
+                                acc[64 + 16 * c + i] = fmaf(__uint_as_float(r[i]), fu, acc[64 + 16 * c + i]);
+                        }
                     }
                 }
                 tc_fence_before();
@@ -274,6 +298,8 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                     buf = 0;
                     tphase ^= 1u;
                 }
+                a0 = a1; g0 = g1; u0 = u1;
+                a1 = a2; g1 = g2; u1 = u2;
             }
             if (!ok) break;
 

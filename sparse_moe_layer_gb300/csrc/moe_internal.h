@@ -17,8 +17,10 @@ struct RouteParams {
     int32_t* topk_idx;
     float* topk_w;
     uint16_t* topk_wb;
-    int32_t* hist;   // [nchunks, E], zeroed before the launch
-    int32_t* done;   // arrival counter, zeroed before the launch
+    int32_t* hist;    // [nchunks, E], zeroed before the launch
+    int32_t* done;    // arrival counter of finished CTAs (or tokens), zeroed before the launch
+    int32_t* tok_cnt; // [T] per-token arrival counters (split-expert path), zeroed before the launch
+    float* logits;    // [T, E] fp32 (split-expert path)
     int32_t* count;
     int32_t* offset;
     int32_t* chunk_base;

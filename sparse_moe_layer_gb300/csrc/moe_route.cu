@@ -12,146 +12,88 @@
 namespace moe {
 
 // ===================================================================== router
-// One CTA (8 warps) per TPB tokens.  The tokens' x rows sit in shared memory;
-// warp w computes the logits of experts w, w+8, ... for all TPB tokens (each
-// router_w row is read once per CTA), fp32 accumulation of bf16 products.
-// Then warp j (< TPB) selects token j's top-k (ties -> lower expert index),
-// stores the k experts in ascending order with the softmax over their k
-// logits (fp32, "softmax after top-k" / "softmax only over the selected
-// experts", weights rounded to bf16), and counts them in the (chunk, expert)
-// histogram.  The last CTA to finish turns the histogram into per-expert
-// row offsets, per-chunk row bases and the GEMM tile lists.
-template <int TPB>
-__global__ void __launch_bounds__(256) router_kernel(RouteParams p) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    const int Hx = (p.H + 7) & ~7;
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
-    float* lg = reinterpret_cast<float*>(smem + (size_t)TPB * Hx * 2);
-    const int t0 = blockIdx.x * TPB;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// a1 + a2 + the histogram half of a3.  logits[t,e] = sum_h x[t,h]*Wr[e,h] +
+// br[e] with bf16 inputs and fp32 accumulation; the k largest (ties -> lower
+// expert index) are stored in ascending expert order with the softmax over
+// their k logits in fp32 ("softmax after top-k", "softmax only over the
+// selected experts"), rounded to bf16 for the combine ("expert weights in
+// bfloat16").  Two kernels compute the logits:
+//   decode-sized T: router_gemv_kernel, one warp per (token, expert), every
+//     load of a warp in flight at once; the last CTA of a token selects;
+//   prefill-sized T: router_mma_kernel, bf16 mma.sync tiles of 32 tokens x
+//     all experts, selection in the same CTA.
+// In both, the last CTA to finish turns the (chunk, expert) histogram into
+// the per-expert row offsets, per-chunk row bases and GEMM tile lists.
 
-    for (int i = threadIdx.x; i < TPB * Hx; i += 256) {
-        int tt = i / Hx, h = i - tt * Hx, t = t0 + tt;
-        xs[i] = (t < p.T && h < p.H) ? p.x[(size_t)t * p.H + h] : (uint16_t)0;
+// The k largest of lg[0..E) for one warp (ties -> lower index), ascending.
+__device__ __forceinline__ void select_topk(const float* lg, int E, int k, int lane, int* chosen) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? lg[e] : -INFINITY;
     }
-    __syncthreads();
-
-    const bool vec = (p.H & 7) == 0;
-    for (int e = warp; e < p.E; e += 8) {
-        float acc[TPB];
-#pragma unroll
-        for (int tt = 0; tt < TPB; ++tt) acc[tt] = 0.f;
-        const uint16_t* wr = p.rw + (size_t)e * p.H;
-        for (int h = lane * 8; h < Hx; h += 256) {
-            float w[8];
-            if (vec) {
-                uint4 v = __ldg(reinterpret_cast<const uint4*>(wr + h));
-                const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    w[2 * i] = __uint_as_float(u[i] << 16);
-                    w[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) w[i] = (h + i < p.H) ? bf16_bits_to_f32(wr[h + i]) : 0.f;
-            }
-#pragma unroll
-            for (int tt = 0; tt < TPB; ++tt) {
-                uint4 v = *reinterpret_cast<const uint4*>(xs + tt * Hx + h);
-                const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[tt] = fmaf(__uint_as_float(u[i] << 16), w[2 * i], acc[tt]);
-                    acc[tt] = fmaf(__uint_as_float(u[i] & 0xffff0000u), w[2 * i + 1], acc[tt]);
-                }
-            }
-        }
-#pragma unroll
-        for (int tt = 0; tt < TPB; ++tt) {
-            float v = acc[tt];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            acc[tt] = v;
-        }
-        if (lane == 0) {
-            const float b = bf16_bits_to_f32(p.rb[e]);
-#pragma unroll
-            for (int tt = 0; tt < TPB; ++tt) lg[tt * p.E + e] = acc[tt] + b;
-        }
-    }
-    __syncthreads();
-
-    if (warp < TPB && t0 + warp < p.T) {
-        const int t = t0 + warp;
-        float v[8];
+    uint32_t taken = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            int e = lane + 32 * i;
-            v[i] = e < p.E ? lg[warp * p.E + e] : -INFINITY;
-        }
-        uint32_t taken = 0;
-        int chosen[kMaxTopK];
-        for (int j = 0; j < p.k; ++j) {
-            float bv = -INFINITY;
-            int be = 0x7fffffff;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                int e = lane + 32 * i;
-                if (e < p.E && !((taken >> i) & 1u) && (be == 0x7fffffff || v[i] > bv)) {
-                    bv = v[i];
-                    be = e;
-                }
+            const int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u) && (be == 0x7fffffff || v[i] > bv)) {
+                bv = v[i];
+                be = e;
             }
+        }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
-                    bv = ov;
-                    be = oe;
-                }
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
+                bv = ov;
+                be = oe;
             }
-            chosen[j] = be;
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
         }
-        // ascending expert order
-        for (int a = 1; a < p.k; ++a) {
-            int key = chosen[a], b = a - 1;
-            while (b >= 0 && chosen[b] > key) {
-                chosen[b + 1] = chosen[b];
-                --b;
-            }
-            chosen[b + 1] = key;
-        }
-        float m = -INFINITY;
-        for (int j = 0; j < p.k; ++j) m = fmaxf(m, lg[warp * p.E + chosen[j]]);
-        float z = 0.f;
-        for (int j = 0; j < p.k; ++j) z += expf(lg[warp * p.E + chosen[j]] - m);
-        if (lane < p.k) {
-            int e = chosen[0];
-#pragma unroll
-            for (int j = 1; j < kMaxTopK; ++j)
-                if (j == lane) e = chosen[j];
-            float w = expf(lg[warp * p.E + e] - m) / z;
-            p.topk_idx[(size_t)t * p.k + lane] = e;
-            p.topk_w[(size_t)t * p.k + lane] = w;
-            __nv_bfloat16 wb = __float2bfloat16_rn(w);
-            p.topk_wb[(size_t)t * p.k + lane] = *reinterpret_cast<uint16_t*>(&wb);
-            atomicAdd(&p.hist[(size_t)(t / kChunkTokens) * p.E + e], 1);
-        }
+        chosen[j] = be;
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
     }
+    for (int a = 1; a < k; ++a) {
+        const int key = chosen[a];
+        int b = a - 1;
+        while (b >= 0 && chosen[b] > key) {
+            chosen[b + 1] = chosen[b];
+            --b;
+        }
+        chosen[b + 1] = key;
+    }
+}
 
-    // ---- last CTA: histogram -> offsets, chunk bases, tile lists ----
-    __shared__ int s_last;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = (atomicAdd(p.done, 1) == (int)gridDim.x - 1);
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
+// Softmax over the chosen logits (fp32, slot order) and the token's outputs;
+// lane j < k writes slot j and counts it in the histogram.
+__device__ __forceinline__ void write_route(const RouteParams& p, int t, const float* lg, const int* chosen,
+                                            int lane) {
+    float m = -INFINITY;
+    for (int j = 0; j < p.k; ++j) m = fmaxf(m, lg[chosen[j]]);
+    float z = 0.f;
+    for (int j = 0; j < p.k; ++j) z += expf(lg[chosen[j]] - m);
+    if (lane < p.k) {
+        int e = chosen[0];
+#pragma unroll
+        for (int j = 1; j < kMaxTopK; ++j)
+            if (j == lane) e = chosen[j];
+        const float w = expf(lg[e] - m) / z;
+        p.topk_idx[(size_t)t * p.k + lane] = e;
+        p.topk_w[(size_t)t * p.k + lane] = w;
+        __nv_bfloat16 wb = __float2bfloat16_rn(w);
+        p.topk_wb[(size_t)t * p.k + lane] = *reinterpret_cast<uint16_t*>(&wb);
+        atomicAdd(&p.hist[(size_t)(t / kChunkTokens) * p.E + e], 1);
+    }
+}
+
+// Run by the last CTA (blockDim 256): counts, offsets, chunk bases, tile lists.
+__device__ void finish_scan(const RouteParams& p) {
     __shared__ int s_count[kMaxExperts], s_off[kMaxExperts];
-    for (int e = threadIdx.x; e < p.E; e += 256) {
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
         int run = 0;
         for (int c = 0; c < p.nchunks; ++c) run += __ldcg(&p.hist[(size_t)c * p.E + e]);
         s_count[e] = run;
@@ -160,11 +102,11 @@ __global__ void __launch_bounds__(256) router_kernel(RouteParams p) {
     if (threadIdx.x == 0) {
         int off = 0, t1 = 0, t2 = 0;
         for (int e = 0; e < p.E; ++e) {
-            int c = s_count[e];
+            const int c = s_count[e];
             s_off[e] = off;
             p.offset[e] = off;
             p.count[e] = c;
-            int mt = (c + 127) / 128;
+            const int mt = (c + 127) / 128;
             p.tiles1[e] = t1;
             p.tiles2[e] = t2;
             off += c;
@@ -178,7 +120,7 @@ __global__ void __launch_bounds__(256) router_kernel(RouteParams p) {
         p.status[kStatusTiles2] = (uint32_t)t2;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < p.E; e += 256) {
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
         int run = s_off[e];
         for (int c = 0; c < p.nchunks; ++c) {
             p.chunk_base[(size_t)c * p.E + e] = run;
@@ -187,17 +129,220 @@ __global__ void __launch_bounds__(256) router_kernel(RouteParams p) {
     }
 }
 
-cudaError_t launch_router(const RouteParams& p, cudaStream_t st) {
+// True in every thread of the CTA that is the `total`-th to arrive on *ctr.
+__device__ __forceinline__ bool last_to_arrive(int* ctr, int total) {
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(ctr, 1) == total - 1);
+    __syncthreads();
+    if (s_last) __threadfence();
+    return s_last != 0;
+}
+
+// ---- decode-sized batches: grid (T, ceil(E/8)), 8 warps, warp = one expert ----
+__global__ void __launch_bounds__(256) router_gemv_kernel(RouteParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // one x row, zero-padded to Hx
     const int Hx = (p.H + 7) & ~7;
-    if (p.T <= 1024) {
-        size_t sm = (size_t)Hx * 2 + (size_t)p.E * 4;
-        cudaFuncSetAttribute(router_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        router_kernel<1><<<p.T, 256, sm, st>>>(p);
+    const int t = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool vec = (p.H & 7) == 0;
+    const uint16_t* xr = p.x + (size_t)t * p.H;
+    if (vec) {
+        for (int i = threadIdx.x; i < Hx / 8; i += 256)
+            reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(xr) + i);
     } else {
-        size_t sm = (size_t)4 * Hx * 2 + (size_t)4 * p.E * 4;
-        cudaFuncSetAttribute(router_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        router_kernel<4><<<(p.T + 3) / 4, 256, sm, st>>>(p);
+        for (int i = threadIdx.x; i < Hx; i += 256) xs[i] = i < p.H ? xr[i] : (uint16_t)0;
     }
+    __syncthreads();
+    const int e = blockIdx.y * 8 + warp;
+    if (e < p.E) {
+        const uint16_t* wr = p.rw + (size_t)e * p.H;
+        float acc = 0.f;
+#pragma unroll 8
+        for (int h = lane * 8; h < Hx; h += 256) {
+            float w[8];
+            if (vec) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(wr + h));
+                const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    w[2 * i] = __uint_as_float(u[i] << 16);
+                    w[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = (h + i < p.H) ? bf16_bits_to_f32(wr[h + i]) : 0.f;
+            }
+            const uint4 xv = *reinterpret_cast<const uint4*>(xs + h);
+            const uint32_t u[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc = fmaf(__uint_as_float(u[i] << 16), w[2 * i], acc);
+                acc = fmaf(__uint_as_float(u[i] & 0xffff0000u), w[2 * i + 1], acc);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) p.logits[(size_t)t * p.E + e] = acc + bf16_bits_to_f32(p.rb[e]);
+    }
+    if (!last_to_arrive(&p.tok_cnt[t], gridDim.y)) return;
+    // this CTA selects token t
+    __shared__ float s_lg[kMaxExperts];
+    for (int i = threadIdx.x; i < p.E; i += 256) s_lg[i] = __ldcg(&p.logits[(size_t)t * p.E + i]);
+    __syncthreads();
+    if (warp == 0) {
+        int chosen[kMaxTopK];
+        select_topk(s_lg, p.E, p.k, lane, chosen);
+        write_route(p, t, s_lg, chosen, lane);
+    }
+    if (last_to_arrive(p.done, p.T)) finish_scan(p);
+}
+
+// ---- prefill-sized batches: 32 tokens x all experts per CTA on bf16 mma.sync ----
+constexpr int kRtTok = 32;   // tokens per CTA
+constexpr int kRtK = 64;     // K chunk
+constexpr int kRtLd = 72;    // padded smem row (bf16 elements): conflict-free fragment loads
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int NTW>  // 8-expert n-tiles per warp; experts padded to EP = 64 * NTW
+__global__ void __launch_bounds__(256) router_mma_kernel(RouteParams p) {
+    constexpr int EP = 64 * NTW;
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                 // [2][kRtTok][kRtLd]
+    uint16_t* ws = xs + 2 * kRtTok * kRtLd;                           // [2][EP][kRtLd]
+    float* lg = reinterpret_cast<float*>(smem);                       // [kRtTok][EP + 4], after the K loop
+    const int t0 = blockIdx.x * kRtTok;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int nchunk = (p.H + kRtK - 1) / kRtK;
+
+    auto load_chunk = [&](int ch, int buf) {
+        const int k0 = ch * kRtK;
+        // x: kRtTok rows x 8 pieces of 16 bytes
+        for (int i = tid; i < kRtTok * 8; i += 256) {
+            const int r = i >> 3, q = i & 7, t = t0 + r, k = k0 + q * 8;
+            const bool ok = t < p.T && k < p.H;
+            cp_async16(smem_u32(xs + (buf * kRtTok + r) * kRtLd + q * 8), ok ? p.x + (size_t)t * p.H + k : p.x, ok);
+        }
+        for (int i = tid; i < EP * 8; i += 256) {
+            const int r = i >> 3, q = i & 7, k = k0 + q * 8;
+            const bool ok = r < p.E && k < p.H;
+            cp_async16(smem_u32(ws + (buf * EP + r) * kRtLd + q * 8), ok ? p.rw + (size_t)r * p.H + k : p.rw, ok);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    float acc[2][NTW][4];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[m][j][q] = 0.f;
+
+    load_chunk(0, 0);
+    for (int ch = 0; ch < nchunk; ++ch) {
+        const int buf = ch & 1;
+        if (ch + 1 < nchunk) {
+            load_chunk(ch + 1, buf ^ 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();
+        const uint16_t* xb = xs + buf * kRtTok * kRtLd;
+        const uint16_t* wb = ws + buf * EP * kRtLd;
+#pragma unroll
+        for (int ks = 0; ks < kRtK / 16; ++ks) {
+            const int kk = ks * 16 + 2 * c;
+            uint32_t a[2][4];
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const uint16_t* r0 = xb + (m * 16 + g) * kRtLd;
+                const uint16_t* r1 = r0 + 8 * kRtLd;
+                a[m][0] = *reinterpret_cast<const uint32_t*>(r0 + kk);
+                a[m][1] = *reinterpret_cast<const uint32_t*>(r1 + kk);
+                a[m][2] = *reinterpret_cast<const uint32_t*>(r0 + kk + 8);
+                a[m][3] = *reinterpret_cast<const uint32_t*>(r1 + kk + 8);
+            }
+#pragma unroll
+            for (int j = 0; j < NTW; ++j) {
+                const uint16_t* br = wb + ((warp * NTW + j) * 8 + g) * kRtLd;
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(br + kk);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(br + kk + 8);
+#pragma unroll
+                for (int m = 0; m < 2; ++m) mma_bf16_16816(acc[m][j], a[m], b0, b1);
+            }
+        }
+        __syncthreads();
+    }
+
+    // logits (+ bias) into shared memory, then one warp per token selects
+    constexpr int LDL = EP + 4;
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int j = 0; j < NTW; ++j) {
+            const int col = (warp * NTW + j) * 8 + 2 * c;
+            const float b0 = col < p.E ? bf16_bits_to_f32(p.rb[col]) : 0.f;
+            const float b1 = col + 1 < p.E ? bf16_bits_to_f32(p.rb[col + 1]) : 0.f;
+            const int row = m * 16 + g;
+            lg[row * LDL + col] = acc[m][j][0] + b0;
+            lg[row * LDL + col + 1] = acc[m][j][1] + b1;
+            lg[(row + 8) * LDL + col] = acc[m][j][2] + b0;
+            lg[(row + 8) * LDL + col + 1] = acc[m][j][3] + b1;
+        }
+    __syncthreads();
+    for (int r = warp; r < kRtTok; r += 8) {
+        const int t = t0 + r;
+        if (t >= p.T) break;
+        int chosen[kMaxTopK];
+        select_topk(lg + r * LDL, p.E, p.k, lane, chosen);
+        write_route(p, t, lg + r * LDL, chosen, lane);
+    }
+    if (last_to_arrive(p.done, gridDim.x)) finish_scan(p);
+}
+
+template <int NTW>
+static cudaError_t launch_router_mma(const RouteParams& p, cudaStream_t st) {
+    constexpr int EP = 64 * NTW;
+    size_t loads = (size_t)2 * (kRtTok + EP) * kRtLd * 2;
+    size_t logit = (size_t)kRtTok * (EP + 4) * 4;
+    size_t sm = loads > logit ? loads : logit;
+    cudaError_t e = cudaFuncSetAttribute(router_mma_kernel<NTW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    router_mma_kernel<NTW><<<(p.T + kRtTok - 1) / kRtTok, 256, sm, st>>>(p);
+    return cudaGetLastError();
+}
+
+bool router_uses_mma(int T, int H) { return T >= 512 && (H % 8) == 0; }
+
+cudaError_t launch_router(const RouteParams& p, cudaStream_t st) {
+    if (router_uses_mma(p.T, p.H)) {
+        if (p.E <= 64) return launch_router_mma<1>(p, st);
+        if (p.E <= 128) return launch_router_mma<2>(p, st);
+        return launch_router_mma<4>(p, st);
+    }
+    const int Hx = (p.H + 7) & ~7;
+    dim3 grid(p.T, (p.E + 7) / 8);
+    size_t sm = (size_t)Hx * 2;
+    cudaError_t e = cudaFuncSetAttribute(router_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    router_gemv_kernel<<<grid, 256, sm, st>>>(p);
     return cudaGetLastError();
 }
 
