@@ -18,7 +18,8 @@
 //               expert's weight rows) per K block into a STAGES-deep ring.
 //   warp 1      TMEM allocator and MMA issuer (one thread): 4 MMAs of K=32
 //               per K block into TMEM buffer kb % NBUF, then commits.
-//   warps 2-9   promotion + epilogue: tcgen05.ld the partial, FMA with the
+//   warps 2-3   idle (they complete warpgroup 0, which gives registers away)
+//   warps 4-11  promotion + epilogue: tcgen05.ld the partial, FMA with the
 //               two scales into registers, release the buffer; after the last
 //               K block run the fused epilogue:
 //                 gate/up GEMM: SwiGLU + 1x128 FP8 requant -> hq, sh
@@ -41,8 +42,13 @@ struct GemmCfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = GATED ? 4 : 6;
     static constexpr int NBUF = 512 / BN;  // TMEM partial buffers (all 512 columns)
-    static constexpr int EPI_WARPS = 8;
-    static constexpr int THREADS = (2 + EPI_WARPS) * 32;
+    static constexpr int EPI_WARPS = 8;                   // warpgroups 1 and 2
+    static constexpr int THREADS = (4 + EPI_WARPS) * 32;  // warpgroup 0: producer, MMA, 2 idle warps
+    // gate/up: the promotion warps hold 128 accumulators + 64 loaded columns, so
+    // warpgroup 0 hands registers to them: 4*32*(168-56) = 8*32*(224-168)
+    static constexpr int LAUNCH_REGS = 168;
+    static constexpr int WG0_REGS = 56;
+    static constexpr int EPI_REGS = 224;
     static constexpr int COLS = BN / 2;  // accumulator columns per epilogue thread
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
     static constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
@@ -94,11 +100,6 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = p.E;
-    for (int i = tid; i <= E; i += C::THREADS) {
-        s_tiles[i] = p.tiles[i];
-        s_off[i] = p.offset[i];
-        if (i < E) s_cnt[i] = p.count[i];
-    }
     if (tid == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
@@ -118,6 +119,14 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), 512);
+    // everything above overlaps the previous kernel's tail; from here on this
+    // kernel reads what the previous kernels wrote
+    pdl_wait();
+    for (int i = tid; i <= E; i += C::THREADS) {
+        s_tiles[i] = p.tiles[i];
+        s_off[i] = p.offset[i];
+        if (i < E) s_cnt[i] = p.count[i];
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -125,7 +134,14 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
     const int total = s_tiles[E];
     volatile int* abort_p = &abort_flag;
     uint32_t* err = p.status + kStatusError;
+    // Every CTA of this persistent grid is resident, so the next kernel may be
+    // scheduled now: its CTAs land on SMs as this grid's CTAs exit and run
+    // their prologue there while the last tiles finish.
+    pdl_allow_dependents();
 
+    if (warp < 4) {
+        if (GATED) regs_release<C::WG0_REGS>();
+    }
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
@@ -213,9 +229,10 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             int dummy = 0;
             mbar_wait(smem_u32(&drain_bar), 0, &dummy, err, kErrTimeoutMma);
         }
-    } else {
+    } else if (warp >= 4) {
         // -------------------------------------------- promotion + epilogue
-        const int ew = warp - 2;
+        if (GATED) regs_acquire<C::EPI_REGS>();
+        const int ew = warp - 4;
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int half = ew >> 2;      // which half of the columns
         const int row = quarter * 32 + lane;
@@ -240,7 +257,7 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             }
             const float* sa_row = p.sa + (size_t)grow_c * p.KB;
             const float* sw_g = p.sw + ((size_t)ti.e * p.sw_rowblocks + ti.nt) * p.KB;
-            const float* sw_u = GATED ? p.sw + ((size_t)ti.e * p.sw_rowblocks + p.up_rows / 128 + ti.nt) * p.KB : sw_g;
+            const int up_off = GATED ? (p.up_rows / 128) * p.KB : 0;  // sw_u = sw_g + up_off
             // Warps whose TMEM lane quarter holds no valid row of this tile only
             // keep the buffer hand-over going (decode tiles have few rows).
             const bool active = quarter * 32 < ti.rows;
@@ -250,11 +267,11 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             if (active) {
                 a0 = __ldg(sa_row);
                 g0 = __ldg(sw_g);
-                if (GATED) u0 = __ldg(sw_u);
+                if (GATED) u0 = __ldg(sw_g + up_off);
                 if (p.KB > 1) {
                     a1 = __ldg(sa_row + 1);
                     g1 = __ldg(sw_g + 1);
-                    if (GATED) u1 = __ldg(sw_u + 1);
+                    if (GATED) u1 = __ldg(sw_g + up_off + 1);
                 }
             }
             for (int kb = 0; kb < p.KB; ++kb) {
@@ -262,7 +279,7 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 if (active && kb + 2 < p.KB) {
                     a2 = __ldg(sa_row + kb + 2);
                     g2 = __ldg(sw_g + kb + 2);
-                    if (GATED) u2 = __ldg(sw_u + kb + 2);
+                    if (GATED) u2 = __ldg(sw_g + up_off + kb + 2);
                 }
                 if (!mbar_wait(smem_u32(&tfull_bar[buf]), tphase, abort_p, err, kErrTimeoutEpilogue)) {
                     ok = false;
@@ -270,25 +287,17 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 }
                 tc_fence_after();
                 if (active) {
-                    const float fg = a0 * g0;
                     const uint32_t tcol = t_lane + (uint32_t)(buf * C::BN);
-                    uint32_t r[16];
+                    uint32_t r[64];
+                    tmem_ld64(tcol + 64 * half, r);
+                    const float fg = a0 * g0;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        tmem_ld16(tcol + 64 * half + 16 * c, r);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            acc[16 * c + i] = fmaf(__uint_as_float(r[i]), fg, acc[16 * c + i]);
-                    }
+                    for (int i = 0; i < 64; ++i) acc[i] = fmaf(__uint_as_float(r[i]), fg, acc[i]);
                     if (GATED) {
+                        tmem_ld64(tcol + 128 + 64 * half, r);
                         const float fu = a0 * u0;
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            tmem_ld16(tcol + 128 + 64 * half + 16 * c, r);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                acc[64 + 16 * c + i] = fmaf(__uint_as_float(r[i]), fu, acc[64 + 16 * c + i]);
-                        }
+                        for (int i = 0; i < 64; ++i) acc[64 + i] = fmaf(__uint_as_float(r[i]), fu, acc[64 + i]);
                     }
                 }
                 tc_fence_before();
@@ -360,11 +369,17 @@ template <bool GATED>
 static cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
                                cudaStream_t st) {
     using C = GemmCfg<GATED>;
+    if (GATED) {
+        // the register hand-over between warpgroups balances only at this launch count
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, moe_gemm_kernel<GATED>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+    }
     cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    moe_gemm_kernel<GATED><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tmA, tmB, p);
-    return cudaGetLastError();
+    return launch_pdl(moe_gemm_kernel<GATED>, dim3(grid), dim3(C::THREADS), (size_t)C::SMEM_BYTES, st, tmA, tmB, p);
 }
 
 cudaError_t launch_gemm_gateup(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace moe {
 
 struct RouteParams {
@@ -62,6 +64,24 @@ struct GemmParams {
     int ldp;
     uint32_t* status;
 };
+
+// Launch with programmatic stream serialisation allowed (the kernel calls
+// griddepcontrol.wait before reading what earlier kernels wrote).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 cudaError_t launch_router(const RouteParams& p, cudaStream_t st);
 cudaError_t launch_permute_quant(const PermuteParams& p, cudaStream_t st);

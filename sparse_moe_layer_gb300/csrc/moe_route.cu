@@ -353,6 +353,7 @@ cudaError_t launch_router(const RouteParams& p, cudaStream_t st) {
 // (token, 128-group) item is quantised by one warp: amax, s = amax/448,
 // code = e4m3(x/s), written to each of the token's k rows.
 __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
+    pdl_wait();
     __shared__ int s_pre[kMaxExperts];
     __shared__ int s_idx[8 * kMaxTopK];
     __shared__ int s_row[8 * kMaxTopK];
@@ -412,8 +413,7 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
 
 cudaError_t launch_permute_quant(const PermuteParams& p, cudaStream_t st) {
     int grid = (p.T + p.tokens_per_cta - 1) / p.tokens_per_cta;
-    permute_quant_kernel<<<grid, 256, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(permute_quant_kernel, dim3(grid), dim3(256), 0, st, p);
 }
 
 // ================================================================= combine
@@ -422,6 +422,7 @@ cudaError_t launch_permute_quant(const PermuteParams& p, cudaStream_t st) {
 // in the down GEMM's epilogue.)
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part, int T, int H, int ldp, int k,
                                                       uint16_t* __restrict__ out) {
+    pdl_wait();
     const int n8 = (H + 7) / 8;
     const size_t total = (size_t)T * n8;
     const bool vec_out = (H & 7) == 0;
@@ -462,8 +463,7 @@ cudaError_t launch_combine(const float* part, int T, int H, int ldp, int k, uint
     size_t cap = (size_t)num_sms * 8;
     int grid = (int)(blocks < cap ? blocks : cap);
     if (grid < 1) grid = 1;
-    combine_kernel<<<grid, 256, 0, st>>>(part, T, H, ldp, k, out);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3(grid), dim3(256), 0, st, part, T, H, ldp, k, out);
 }
 
 // ============================================================ weight packer

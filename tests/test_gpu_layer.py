@@ -47,7 +47,12 @@ def full_check(moe, layer: Layer, n_sample: int | None = None):
     r = layer.oracle_router()
     # routing: bit-exact indices, weights within one bf16 step
     assert np.array_equal(v["topk_idx"].cpu().numpy(), r["idx"])
-    assert np.allclose(v["topk_w"].cpu().numpy(), r["w_f32"], rtol=2e-6, atol=1e-7)
+    # fp32 softmax weights: |dw|/w <= 2*|d logit|; the GPU logits (fp32 FMA or tensor-core
+    # accumulation of H bf16 products) are within ~2.5e-5 of the fp64 ones for H <= 4096
+    w_gpu = v["topk_w"].cpu().numpy()
+    wrel = np.abs(w_gpu - r["w_f32"]) / r["w_f32"]
+    print(f"routing weight max rel diff {wrel.max():.3g}")
+    assert wrel.max() <= 5e-5
     wb_gpu = v["topk_wb"].cpu().view(torch.int16).numpy().view(np.uint16).astype(np.int32)
     assert np.all(np.abs(wb_gpu - r["w_bf16"].astype(np.int32)) <= 1)
     # grouping by expert: bit-exact
