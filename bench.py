@@ -153,9 +153,9 @@ def build_layer(cfg, device):
     rw, rb = synth.router(cfg)
     b13, b2 = synth.expert_biases(cfg)
     E, H, I, Hp, Ip = cfg.E, cfg.H, cfg.I, cfg.Hp, cfg.Ip
-    w13 = torch.empty((E, 2 * Ip, Hp), dtype=torch.uint8, device=device)
+    w13 = torch.empty(moe.w13_shape(E, H, I), dtype=torch.uint8, device=device)
     s13 = torch.empty((E, 2 * Ip // 128, Hp // 128), dtype=torch.float32, device=device)
-    w2 = torch.empty((E, Hp, Ip), dtype=torch.uint8, device=device)
+    w2 = torch.empty(moe.w2_shape(E, H, I), dtype=torch.uint8, device=device)
     s2 = torch.empty((E, Hp // 128, Ip // 128), dtype=torch.float32, device=device)
     chunk = 8
     for e0 in range(0, E, chunk):
@@ -348,6 +348,9 @@ def main():
     torch.cuda.synchronize()
     for i in range(K):
         flush.fill_(i & 0xFF)
+        # a ~0.1 ms spin kernel lets the host enqueue the whole step before its
+        # first event, so no stage time contains host launch latency
+        torch.cuda._sleep(200_000)
         moe.forward(x_dev, layer.router_w, layer.router_b, layer.w13, layer.s13, layer.b13, layer.w2, layer.s2,
                     layer.b2, cfg.top_k, out=out, workspace=ws, events=ev[i])
     torch.cuda.synchronize()

@@ -20,10 +20,14 @@
  *   out[t,:]    = bf16( sum_j w[t,j] * y[t,j,:] )    (slot order, no atomics)
  *
  * Padding rule (sizes that are not multiples of 128, e.g. 2880):
- *   Hp = ceil(H/128)*128, Ip = ceil(I/128)*128.  w13 is [E, 2*Ip, Hp] e4m3
- *   with gate rows at [0, I) and up rows at [Ip, Ip+I); w2 is [E, Hp, Ip];
- *   every padded row/column holds code 0; block scales cover the padded
- *   128x128 blocks (use moe_pack_weights to build them).
+ *   Hp = ceil(H/128)*128, Ip = ceil(I/128)*128.  Logically w13 is
+ *   [E, 2*Ip, Hp] e4m3 with gate rows at [0, I) and up rows at [Ip, Ip+I), and
+ *   w2 is [E, Hp, Ip]; every padded row/column holds code 0; block scales
+ *   cover the padded 128x128 blocks.  In memory the codes are BLOCKED: each
+ *   128x128 block is 16 KB contiguous (row-major inside), blocks ordered
+ *   [expert][row block][column block], i.e. w13 is [E, 2*Ip/128, Hp/128,
+ *   128, 128] and w2 is [E, Hp/128, Ip/128, 128, 128], so a GEMM tile is one
+ *   contiguous HBM read.  moe_pack_weights builds this layout.
  *
  * Ownership: the caller owns every buffer, including the workspace.  Calls
  * never allocate device memory, never synchronise the stream (except
@@ -78,9 +82,9 @@ typedef struct {
     size_t perm;       /* int32 [R] row r -> t*top_k + j; rows sorted by (expert, token) */
     size_t inv;        /* int32 [R] t*top_k + j -> row */
     size_t xq;         /* e4m3  [R, Hp] quantised x, permuted rows */
-    size_t sx;         /* float [R, Hp/128] */
+    size_t sx;         /* float [Hp/128, R] group scales of xq, K-block-major */
     size_t hq;         /* e4m3  [R, Ip] requantised h */
-    size_t sh;         /* float [R, Ip/128] */
+    size_t sh;         /* float [Ip/128, R] group scales of hq, K-block-major */
     size_t part;       /* float [R, Hp] w[t,j]*y rows, indexed by t*top_k + j */
 } moe_workspace_layout;
 
@@ -93,9 +97,9 @@ moe_status moe_get_workspace_layout(int T, int H, int I, int E, int top_k, moe_w
 /*
  * The layer forward.
  *   x        bf16 [T, H] row-major          router_w bf16 [E, H]    router_b bf16 [E]
- *   w13      e4m3 [E, 2*Ip, Hp]             s13 fp32 [E, 2*Ip/128, Hp/128]
+ *   w13      e4m3 blocked [E, 2*Ip/128, Hp/128, 128, 128]   s13 fp32 [E, 2*Ip/128, Hp/128]
  *   b13      bf16 [E, 2*I]  (gate [0,I), up [I,2I))
- *   w2       e4m3 [E, Hp, Ip]               s2  fp32 [E, Hp/128, Ip/128]
+ *   w2       e4m3 blocked [E, Hp/128, Ip/128, 128, 128]     s2  fp32 [E, Hp/128, Ip/128]
  *   b2       bf16 [E, H]
  *   out      bf16 [T, H]
  *   workspace: device buffer of at least moe_workspace_size(...) bytes, 256-byte aligned.
@@ -121,7 +125,8 @@ moe_status moe_forward_profiled(const void* x, const void* router_w, const void*
  * Weight packer (the offline converter from master weights to the layer's
  * FP8 layout; "GPT-OSS on Day 0": FP8 with 128x128 block scaling).
  *   w13_f32 fp32 [E, 2*I, H] (gate rows then up rows), w2_f32 fp32 [E, H, I]  (device)
- *   -> w13 e4m3 [E, 2*Ip, Hp], s13 [E, 2*Ip/128, Hp/128], w2 e4m3 [E, Hp, Ip], s2 [E, Hp/128, Ip/128]
+ *   -> w13 e4m3 blocked [E, 2*Ip/128, Hp/128, 128, 128], s13 [E, 2*Ip/128, Hp/128],
+ *      w2 e4m3 blocked [E, Hp/128, Ip/128, 128, 128], s2 [E, Hp/128, Ip/128]
  * Each 128x128 block: s = amax/448 (1 when the block is all zero), code =
  * e4m3_rne_satfinite(w/s) in IEEE fp32; padding gets code 0.
  * Either input may be NULL to pack only the other matrix.

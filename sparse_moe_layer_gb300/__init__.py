@@ -16,7 +16,8 @@ import torch
 from .build import LIB, build
 
 __all__ = ["MoeError", "build", "lib", "workspace_size", "workspace_layout", "workspace_views", "forward",
-           "pack_weights", "quantize_rows", "read_device_status", "test_bounded_wait", "MoeLayer", "pad128"]
+           "pack_weights", "pack_weights_into", "w13_shape", "w2_shape", "unblock", "quantize_rows",
+           "read_device_status", "test_bounded_wait", "MoeLayer", "pad128"]
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "CUDA error",
           5: "device wait timed out"}
@@ -136,9 +137,9 @@ def workspace_views(ws: torch.Tensor, T: int, H: int, I: int, E: int, top_k: int
         perm=v("perm", R, torch.int32, (R,)),
         inv=v("inv", R, torch.int32, (R,)),
         xq=v("xq", R * Hp, torch.uint8, (R, Hp)),
-        sx=v("sx", R * Hp // 128, torch.float32, (R, Hp // 128)),
+        sx=v("sx", R * Hp // 128, torch.float32, (Hp // 128, R)).t(),  # stored K-block-major
         hq=v("hq", R * Ip, torch.uint8, (R, Ip)),
-        sh=v("sh", R * Ip // 128, torch.float32, (R, Ip // 128)),
+        sh=v("sh", R * Ip // 128, torch.float32, (Ip // 128, R)).t(),
         part=v("part", R * Hp, torch.float32, (R, Hp)),
     )
 
@@ -156,7 +157,7 @@ def forward(x, router_w, router_b, w13, s13, b13, w2, s2, b2, top_k: int, out=No
     E = router_w.shape[0]
     I = b13.shape[1] // 2
     Hp, Ip = pad128(H), pad128(I)
-    if tuple(w13.shape) != (E, 2 * Ip, Hp) or tuple(w2.shape) != (E, Hp, Ip):
+    if tuple(w13.shape) != w13_shape(E, H, I) or tuple(w2.shape) != w2_shape(E, H, I):
         raise ValueError(f"packed weight shapes {tuple(w13.shape)}, {tuple(w2.shape)} do not match H={H} I={I} E={E}")
     if tuple(s13.shape) != (E, 2 * Ip // 128, Hp // 128) or tuple(s2.shape) != (E, Hp // 128, Ip // 128):
         raise ValueError("block scale shapes do not match")
@@ -181,6 +182,22 @@ def forward(x, router_w, router_b, w13, s13, b13, w2, s2, b2, top_k: int, out=No
     return out
 
 
+def w13_shape(E: int, H: int, I: int) -> tuple:
+    """Packed gate/up codes: blocked [E, 2*Ip/128, Hp/128, 128, 128] (each 128x128 block contiguous)."""
+    return (E, 2 * pad128(I) // 128, pad128(H) // 128, 128, 128)
+
+
+def w2_shape(E: int, H: int, I: int) -> tuple:
+    """Packed down codes: blocked [E, Hp/128, Ip/128, 128, 128]."""
+    return (E, pad128(H) // 128, pad128(I) // 128, 128, 128)
+
+
+def unblock(q: torch.Tensor) -> torch.Tensor:
+    """Blocked codes [E, RB, KB, 128, 128] -> row-major [E, RB*128, KB*128] (for inspection)."""
+    E, RB, KB = q.shape[:3]
+    return q.permute(0, 1, 3, 2, 4).reshape(E, RB * 128, KB * 128)
+
+
 def pack_weights(w13_f32: torch.Tensor, w2_f32: torch.Tensor, stream=None, out=None):
     """fp32 masters w13 [E, 2I, H], w2 [E, H, I] -> (w13 e4m3 codes, s13, w2 codes, s2) in the layer's layout."""
     E, twoI, H = w13_f32.shape
@@ -188,9 +205,9 @@ def pack_weights(w13_f32: torch.Tensor, w2_f32: torch.Tensor, stream=None, out=N
     Hp, Ip = pad128(H), pad128(I)
     dev = w13_f32.device
     if out is None:
-        out = (torch.empty((E, 2 * Ip, Hp), dtype=torch.uint8, device=dev),
+        out = (torch.empty(w13_shape(E, H, I), dtype=torch.uint8, device=dev),
                torch.empty((E, 2 * Ip // 128, Hp // 128), dtype=torch.float32, device=dev),
-               torch.empty((E, Hp, Ip), dtype=torch.uint8, device=dev),
+               torch.empty(w2_shape(E, H, I), dtype=torch.uint8, device=dev),
                torch.empty((E, Hp // 128, Ip // 128), dtype=torch.float32, device=dev))
     q13, s13, q2, s2 = out
     if tuple(w2_f32.shape) != (E, H, I):

@@ -75,13 +75,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     return g_encode;
 }
 
-// 2D uint8 tensor [rows, cols] (row stride = cols bytes), box 128 x 128, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+// 2D uint8 tensor [rows, cols] (row stride = cols bytes), box 128 bytes x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows = 128) {
     auto enc = encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols};
-    cuuint32_t box[2] = {128, 128};
+    cuuint32_t box[2] = {128, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -182,6 +182,9 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     rp.nchunks = nch;
     rp.nt1 = Ip / 128;
     rp.nt2 = Hp / 128;
+    // Few rows per expert (decode): weight-streaming kernels with 32-row token tiles.
+    const bool decode = (long long)R <= 64LL * E;
+    rp.bm = decode ? 32 : 128;
     rp.topk_idx = reinterpret_cast<int32_t*>(ws + L.topk_idx);
     rp.topk_w = reinterpret_cast<float*>(ws + L.topk_w);
     rp.topk_wb = reinterpret_cast<uint16_t*>(ws + L.topk_wb);
@@ -211,16 +214,18 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     pp.perm = reinterpret_cast<int32_t*>(ws + L.perm);
     pp.inv = reinterpret_cast<int32_t*>(ws + L.inv);
     pp.xq = ws + L.xq;
+    pp.R = R;
     pp.sx = reinterpret_cast<float*>(ws + L.sx);
     if (launch_permute_quant(pp, st) != cudaSuccess) return MOE_ERR_CUDA;
     mark(2);
 
-    // upper bound of the tile count of either GEMM: sum_e ceil(count_e/128) <= E + R/128
-    const long long mt_bound = (long long)E + (R + 127) / 128;
+    // upper bound of the tile count of either GEMM: sum_e ceil(count_e/bm) <= E + R/bm
+    const long long mt_bound = (long long)E + (R + rp.bm - 1) / rp.bm;
 
     CUtensorMap tmA1, tmB1, tmA2, tmB2;
-    if (!make_map(&tmA1, pp.xq, R, Hp) || !make_map(&tmB1, w13, (uint64_t)E * 2 * Ip, Hp) ||
-        !make_map(&tmA2, ws + L.hq, R, Ip) || !make_map(&tmB2, w2, (uint64_t)E * Hp, Ip))
+    // weights are blocked: a 2D view of 128-byte rows, one 128x128 block = 128 consecutive rows
+    if (!make_map(&tmA1, pp.xq, R, Hp, rp.bm) || !make_map(&tmB1, w13, (uint64_t)E * 2 * Ip * (Hp / 128), 128) ||
+        !make_map(&tmA2, ws + L.hq, R, Ip, rp.bm) || !make_map(&tmB2, w2, (uint64_t)E * Hp * (Ip / 128), 128))
         return MOE_ERR_CUDA;
 
     GemmParams g1;
@@ -244,7 +249,9 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     g1.status = rp.status;
     long long t1 = mt_bound * (Ip / 128);
     int grid1 = (int)(t1 < sms ? t1 : sms);
-    if (launch_gemm_gateup(tmA1, tmB1, g1, grid1, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if ((decode ? launch_gemm_gateup_decode(tmB1, tmA1, g1, grid1, st) : launch_gemm_gateup(tmA1, tmB1, g1, grid1, st))
+        != cudaSuccess)
+        return MOE_ERR_CUDA;
     mark(3);
 
     GemmParams g2;
@@ -269,7 +276,9 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     g2.status = rp.status;
     long long t2 = mt_bound * (Hp / 128);
     int grid2 = (int)(t2 < sms ? t2 : sms);
-    if (launch_gemm_down(tmA2, tmB2, g2, grid2, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if ((decode ? launch_gemm_down_decode(tmB2, tmA2, g2, grid2, st) : launch_gemm_down(tmA2, tmB2, g2, grid2, st)) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
     mark(4);
 
     if (launch_combine(g2.part, T, H, Hp, top_k, static_cast<uint16_t*>(out), sms, st) != cudaSuccess)

@@ -51,7 +51,8 @@ struct GemmCfg {
     static constexpr int EPI_REGS = 224;
     static constexpr int COLS = BN / 2;  // accumulator columns per epilogue thread
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
-    static constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
+    static constexpr uint32_t IDESC = idesc_e4m3_f32(BM, 128);  // one MMA half: 128 columns
+    static constexpr int HALVES = BN / 128;                      // gate/up: 2 halves with their own barriers
 };
 
 struct TileInfo {
@@ -89,8 +90,8 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
 
     __shared__ __align__(8) uint64_t full_bar[C::STAGES];
     __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
-    __shared__ __align__(8) uint64_t tfull_bar[C::NBUF];
-    __shared__ __align__(8) uint64_t tempty_bar[C::NBUF];
+    __shared__ __align__(8) uint64_t tfull_bar[C::NBUF][C::HALVES];
+    __shared__ __align__(8) uint64_t tempty_bar[C::NBUF][C::HALVES];
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ __align__(8) uint64_t amax_bar;  // gate/up epilogue: the two column halves of a row meet here
     __shared__ uint32_t tmem_slot;
@@ -105,10 +106,11 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
         }
-        for (int b = 0; b < C::NBUF; ++b) {
-            mbar_init(smem_u32(&tfull_bar[b]), 1);
-            mbar_init(smem_u32(&tempty_bar[b]), C::EPI_WARPS);
-        }
+        for (int b = 0; b < C::NBUF; ++b)
+            for (int h = 0; h < C::HALVES; ++h) {
+                mbar_init(smem_u32(&tfull_bar[b][h]), 1);
+                mbar_init(smem_u32(&tempty_bar[b][h]), C::EPI_WARPS);
+            }
         mbar_init(smem_u32(&drain_bar), 1);
         mbar_init(smem_u32(&amax_bar), C::EPI_WARPS * 32);
         abort_flag = 0;
@@ -151,7 +153,9 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const TileInfo ti = decode_tile(tile, s_tiles, s_off, s_cnt, E);
-                const int brow = ti.e * p.rows_B + ti.nt * 128;
+                // blocked weights: block (e, row block, kb) starts at row ((e*RB + rb)*KB + kb)*128
+                const int bblk = (ti.e * p.sw_rowblocks + ti.nt) * p.KB;
+                const int ublk = GATED ? (p.up_rows / 128) * p.KB : 0;
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) {
                         ok = false;
@@ -162,8 +166,8 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                     const uint32_t a_dst = smem_u32(smem + stage * C::STAGE_BYTES);
                     const uint32_t b_dst = a_dst + C::A_BYTES;
                     tma_load_2d(a_dst, &tmA, kb * 128, ti.row0, fb);
-                    tma_load_2d(b_dst, &tmB, kb * 128, brow, fb);
-                    if (GATED) tma_load_2d(b_dst + 128 * 128, &tmB, kb * 128, brow + p.up_rows, fb);
+                    tma_load_2d(b_dst, &tmB, 0, (bblk + kb) * 128, fb);
+                    if (GATED) tma_load_2d(b_dst + 128 * 128, &tmB, 0, (bblk + ublk + kb) * 128, fb);
                     filled |= 1u << stage;
                     if (++stage == C::STAGES) {
                         stage = 0;
@@ -198,22 +202,32 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             uint32_t sphase = 0, tphase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                for (int kb = 0; kb < p.KB; ++kb) {
-                    if (!mbar_wait(smem_u32(&full_bar[stage]), sphase, abort_p, err, kErrTimeoutMma) ||
-                        !mbar_wait(smem_u32(&tempty_bar[buf]), tphase ^ 1u, abort_p, err, kErrTimeoutMma)) {
+                for (int kb = 0; kb < p.KB && ok; ++kb) {
+                    if (!mbar_wait(smem_u32(&full_bar[stage]), sphase, abort_p, err, kErrTimeoutMma)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
                     const uint32_t a_base = smem_u32(smem + stage * C::STAGE_BYTES);
                     const uint32_t b_base = a_base + C::A_BYTES;
-                    const uint32_t d = tmem_base + (uint32_t)(buf * C::BN);
+                    // gate/up: the gate half and the up half of the accumulator are
+                    // handed to the promotion warps separately, so one half is
+                    // promoted while the tensor core works on the other
 #pragma unroll
-                    for (int k4 = 0; k4 < 4; ++k4)
-                        mma_e4m3(d, smem_desc_sw128(a_base + 32 * k4), smem_desc_sw128(b_base + 32 * k4), C::IDESC,
-                                 k4 > 0 ? 1u : 0u);
+                    for (int h = 0; h < C::HALVES; ++h) {
+                        if (!mbar_wait(smem_u32(&tempty_bar[buf][h]), tphase ^ 1u, abort_p, err, kErrTimeoutMma)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d = tmem_base + (uint32_t)(buf * C::BN + 128 * h);
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            mma_e4m3(d, smem_desc_sw128(a_base + 32 * k4), smem_desc_sw128(b_base + 128 * 128 * h + 32 * k4),
+                                     C::IDESC, k4 > 0 ? 1u : 0u);
+                        mma_commit(smem_u32(&tfull_bar[buf][h]));
+                    }
+                    if (!ok) break;
                     mma_commit(smem_u32(&empty_bar[stage]));
-                    mma_commit(smem_u32(&tfull_bar[buf]));
                     if (++stage == C::STAGES) {
                         stage = 0;
                         sphase ^= 1u;
@@ -255,7 +269,7 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 acc[i] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + n)) : 0.f;
                 if (GATED) acc[64 + i] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + p.N_real + n)) : 0.f;
             }
-            const float* sa_row = p.sa + (size_t)grow_c * p.KB;
+            const float* sa_row = p.sa + grow_c;  // element kb at sa_row[kb * R]
             const float* sw_g = p.sw + ((size_t)ti.e * p.sw_rowblocks + ti.nt) * p.KB;
             const int up_off = GATED ? (p.up_rows / 128) * p.KB : 0;  // sw_u = sw_g + up_off
             // Warps whose TMEM lane quarter holds no valid row of this tile only
@@ -269,7 +283,7 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 g0 = __ldg(sw_g);
                 if (GATED) u0 = __ldg(sw_g + up_off);
                 if (p.KB > 1) {
-                    a1 = __ldg(sa_row + 1);
+                    a1 = __ldg(sa_row + (size_t)p.R);
                     g1 = __ldg(sw_g + 1);
                     if (GATED) u1 = __ldg(sw_g + up_off + 1);
                 }
@@ -277,32 +291,33 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             for (int kb = 0; kb < p.KB; ++kb) {
                 float a2 = 0.f, g2 = 0.f, u2 = 0.f;
                 if (active && kb + 2 < p.KB) {
-                    a2 = __ldg(sa_row + kb + 2);
+                    a2 = __ldg(sa_row + (size_t)(kb + 2) * p.R);
                     g2 = __ldg(sw_g + kb + 2);
                     if (GATED) u2 = __ldg(sw_g + up_off + kb + 2);
                 }
-                if (!mbar_wait(smem_u32(&tfull_bar[buf]), tphase, abort_p, err, kErrTimeoutEpilogue)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (active) {
-                    const uint32_t tcol = t_lane + (uint32_t)(buf * C::BN);
-                    uint32_t r[64];
-                    tmem_ld64(tcol + 64 * half, r);
-                    const float fg = a0 * g0;
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) acc[i] = fmaf(__uint_as_float(r[i]), fg, acc[i]);
-                    if (GATED) {
-                        tmem_ld64(tcol + 128 + 64 * half, r);
-                        const float fu = a0 * u0;
-#pragma unroll
-                        for (int i = 0; i < 64; ++i) acc[64 + i] = fmaf(__uint_as_float(r[i]), fu, acc[64 + i]);
+                for (int h = 0; h < C::HALVES; ++h) {
+                    if (!mbar_wait(smem_u32(&tfull_bar[buf][h]), tphase, abort_p, err, kErrTimeoutEpilogue)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    if (active) {
+                        uint32_t r[64];
+                        tmem_ld64(t_lane + (uint32_t)(buf * C::BN + 128 * h + 64 * half), r);
+                        const float f = a0 * (h == 0 ? g0 : u0);
+                        const float2 f2 = make_float2(f, f);
+                        float2* a2p = reinterpret_cast<float2*>(acc + 64 * h);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            a2p[i] = __ffma2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), f2,
+                                                a2p[i]);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[buf][h]));
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[buf]));
+                if (!ok) break;
                 if (++buf == C::NBUF) {
                     buf = 0;
                     tphase ^= 1u;
@@ -342,7 +357,7 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                         }
                         dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
-                    if (half == 0) p.sh[(size_t)grow * (p.ldq / 128) + ti.nt] = s;
+                    if (half == 0) p.sh[(size_t)ti.nt * p.R + grow] = s;
                 }
             } else {
                 if (valid) {

@@ -1,0 +1,363 @@
+// Grouped FP8 expert GEMMs for decode-sized batches (few rows per expert).
+//
+// Same arithmetic as the prefill kernels (moe_gemm.cu):
+//   acc[r, n] = bias[n] + sum_kb (sa[kb, r] * sw[n/128, kb]) * P_kb[r, n]
+// but with the operands swapped: the expert's weight rows are the MMA's M=128
+// operand and at most 32 token rows of that expert are the N=32 operand, so
+// TMEM holds acc^T (lane = output feature, column = token).  Decode is bound
+// by streaming the activated experts' weights from HBM ("Hosting Qwen on
+// Blackwell", Decoders: with few tokens the GEMM is limited by loading
+// weights into the tensor cores), so nearly all of every pipeline stage is
+// weight bytes: 5 stages of 32 KB (gate + up) or 10 of 16 KB (down) are in
+// flight per SM, and the small TMEM tiles give 4-8 accumulation buffers, so
+// the scale promotion never stalls the MMA.
+//
+// Tile = (expert, 128 output features, 32 token rows), ordered expert,
+// n-tile, m-tile; one CTA per SM, persistent.
+//   warp 0     TMA producer (weights: one or two 128x128 boxes; tokens: one 32x128 box)
+//   warp 1     TMEM allocator and MMA issuer
+//   warps 2-5  promotion + epilogue, one TMEM lane quarter (32 features) each:
+//              gate/up: h = silu(g)*u, 1x128 requant across the 128 features of
+//              a token (warp shuffles + shared memory), codes -> hq, scales -> sh
+//              down: * routing weight -> part[t*k+j, n]
+#include <cuda_bf16.h>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+template <bool GATED>
+struct DecCfg {
+    static constexpr int BT = 32;                         // token rows per tile (MMA N)
+    static constexpr int W_BYTES = (GATED ? 2 : 1) * 128 * 128;
+    static constexpr int X_BYTES = BT * 128;
+    static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
+    static constexpr int STAGES = GATED ? 5 : 10;
+    static constexpr int ACC_COLS = GATED ? 2 * BT : BT;  // TMEM columns of one accumulation buffer
+    static constexpr int TMEM_COLS = 256;
+    static constexpr int NBUF = TMEM_COLS / ACC_COLS;     // 4 (gate/up) or 8 (down)
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int THREADS = (2 + EPI_WARPS) * 32;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+    static constexpr uint32_t IDESC = idesc_e4m3_f32(128, BT);
+};
+
+struct DecTile {
+    int e, nt, row0, rows;
+};
+
+__device__ __forceinline__ DecTile decode_dec_tile(int tile, const int* s_tiles, const int* s_off, const int* s_cnt,
+                                                   int E) {
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_tiles[mid] <= tile)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    DecTile ti;
+    ti.e = lo;
+    const int local = tile - s_tiles[lo];
+    const int mtc = (s_cnt[lo] + 31) >> 5;
+    ti.nt = local / mtc;
+    const int mt = local - ti.nt * mtc;
+    ti.row0 = s_off[lo] + mt * 32;
+    ti.rows = min(32, s_cnt[lo] - mt * 32);
+    return ti;
+}
+
+template <bool GATED>
+__global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
+    moe_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                           const GemmParams p) {
+    using C = DecCfg<GATED>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+
+    __shared__ __align__(8) uint64_t full_bar[C::STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
+    __shared__ __align__(8) uint64_t tfull_bar[C::NBUF];
+    __shared__ __align__(8) uint64_t tempty_bar[C::NBUF];
+    __shared__ __align__(8) uint64_t drain_bar;
+    __shared__ __align__(8) uint64_t amax_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    __shared__ int s_tiles[kMaxExperts + 1], s_off[kMaxExperts + 1], s_cnt[kMaxExperts];
+    __shared__ float s_amax[2][4][32];  // [tile parity][lane quarter][token]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int E = p.E;
+    if (tid == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int b = 0; b < C::NBUF; ++b) {
+            mbar_init(smem_u32(&tfull_bar[b]), 1);
+            mbar_init(smem_u32(&tempty_bar[b]), C::EPI_WARPS);
+        }
+        mbar_init(smem_u32(&drain_bar), 1);
+        mbar_init(smem_u32(&amax_bar), C::EPI_WARPS * 32);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmX);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), C::TMEM_COLS);
+    pdl_wait();
+    for (int i = tid; i <= E; i += C::THREADS) {
+        s_tiles[i] = p.tiles[i];
+        s_off[i] = p.offset[i];
+        if (i < E) s_cnt[i] = p.count[i];
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_slot;
+    const int total = s_tiles[E];
+    volatile int* abort_p = &abort_flag;
+    uint32_t* err = p.status + kStatusError;
+    pdl_allow_dependents();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0, filled = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const DecTile ti = decode_dec_tile(tile, s_tiles, s_off, s_cnt, E);
+                // blocked weights: block (e, row block, kb) starts at row ((e*RB + rb)*KB + kb)*128
+                const int wblk = (ti.e * p.sw_rowblocks + ti.nt) * p.KB;
+                const int ublk = GATED ? (p.up_rows / 128) * p.KB : 0;
+                for (int kb = 0; kb < p.KB; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full_bar[stage]);
+                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    const uint32_t w_dst = smem_u32(smem + stage * C::STAGE_BYTES);
+                    tma_load_2d(w_dst, &tmW, 0, (wblk + kb) * 128, fb);
+                    if (GATED) tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb) * 128, fb);
+                    tma_load_2d(w_dst + C::W_BYTES, &tmX, kb * 128, ti.row0, fb);
+                    filled |= 1u << stage;
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            int dummy = 0;
+            for (int i = 0; i < C::STAGES; ++i) {
+                const int s = (stage + C::STAGES - 1 - i) % C::STAGES;
+                const uint32_t ph = (s < stage) ? phase : phase ^ 1u;
+                if (filled & (1u << s)) mbar_wait(smem_u32(&full_bar[s]), ph, &dummy, err, kErrTimeoutProducer);
+            }
+            if (ok) {
+                for (int i = 0; i < C::STAGES; ++i) {
+                    if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) break;
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------- MMA issuer
+            int stage = 0, buf = 0;
+            uint32_t sphase = 0, tphase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                for (int kb = 0; kb < p.KB; ++kb) {
+                    if (!mbar_wait(smem_u32(&full_bar[stage]), sphase, abort_p, err, kErrTimeoutMma) ||
+                        !mbar_wait(smem_u32(&tempty_bar[buf]), tphase ^ 1u, abort_p, err, kErrTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t w_base = smem_u32(smem + stage * C::STAGE_BYTES);
+                    const uint32_t x_base = w_base + C::W_BYTES;
+                    const uint32_t d = tmem_base + (uint32_t)(buf * C::ACC_COLS);
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const uint64_t xd = smem_desc_sw128(x_base + 32 * k4);
+                        mma_e4m3(d, smem_desc_sw128(w_base + 32 * k4), xd, C::IDESC, k4 > 0 ? 1u : 0u);
+                        if (GATED)
+                            mma_e4m3(d + C::BT, smem_desc_sw128(w_base + 128 * 128 + 32 * k4), xd, C::IDESC,
+                                     k4 > 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&empty_bar[stage]));
+                    mma_commit(smem_u32(&tfull_bar[buf]));
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        sphase ^= 1u;
+                    }
+                    if (++buf == C::NBUF) {
+                        buf = 0;
+                        tphase ^= 1u;
+                    }
+                }
+            }
+            mma_commit(smem_u32(&drain_bar));
+            int dummy = 0;
+            mbar_wait(smem_u32(&drain_bar), 0, &dummy, err, kErrTimeoutMma);
+        }
+    } else {
+        // -------------------------------------------- promotion + epilogue
+        const int quarter = warp & 3;            // TMEM lanes this warp may access
+        const int nl = quarter * 32 + lane;      // output feature within the 128-wide n-tile
+        const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
+        int buf = 0;
+        uint32_t tphase = 0, tpar = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, tpar ^= 1u) {
+            const DecTile ti = decode_dec_tile(tile, s_tiles, s_off, s_cnt, E);
+            const int n = ti.nt * 128 + nl;
+            const bool nvalid = n < p.N_real;
+            float acc[C::ACC_COLS];
+            {
+                const uint16_t* bias_e = p.bias + (size_t)ti.e * (GATED ? 2 * p.N_real : p.N_real);
+                const float bg = nvalid ? bf16_bits_to_f32(__ldg(bias_e + n)) : 0.f;
+                const float bu = (GATED && nvalid) ? bf16_bits_to_f32(__ldg(bias_e + p.N_real + n)) : 0.f;
+#pragma unroll
+                for (int j = 0; j < C::BT; ++j) {
+                    acc[j] = bg;
+                    if (GATED) acc[C::BT + j] = bu;
+                }
+            }
+            // this lane's token: scales of K blocks kb, kb+1 in registers, kb+2 loading
+            const int rtok = min(ti.row0 + lane, p.R - 1);
+            const float* sa_col = p.sa + rtok;  // element kb at sa_col[kb * R]
+            const float* sw_g = p.sw + ((size_t)ti.e * p.sw_rowblocks + ti.nt) * p.KB;
+            const int up_off = GATED ? (p.up_rows / 128) * p.KB : 0;
+            float a0 = __ldg(sa_col), g0 = __ldg(sw_g), u0 = GATED ? __ldg(sw_g + up_off) : 0.f;
+            float a1 = 0.f, g1 = 0.f, u1 = 0.f;
+            if (p.KB > 1) {
+                a1 = __ldg(sa_col + (size_t)p.R);
+                g1 = __ldg(sw_g + 1);
+                if (GATED) u1 = __ldg(sw_g + up_off + 1);
+            }
+            for (int kb = 0; kb < p.KB; ++kb) {
+                float a2 = 0.f, g2 = 0.f, u2 = 0.f;
+                if (kb + 2 < p.KB) {
+                    a2 = __ldg(sa_col + (size_t)(kb + 2) * p.R);
+                    g2 = __ldg(sw_g + kb + 2);
+                    if (GATED) u2 = __ldg(sw_g + up_off + kb + 2);
+                }
+                if (!mbar_wait(smem_u32(&tfull_bar[buf]), tphase, abort_p, err, kErrTimeoutEpilogue)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tcol = t_lane + (uint32_t)(buf * C::ACC_COLS);
+                const float fg = a0 * g0;  // lane j: scale of token j for the gate (or down) rows
+                const float fu = a0 * u0;
+                if (GATED) {
+                    uint32_t r[64];
+                    tmem_ld64(tcol, r);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float sg = __shfl_sync(0xffffffffu, fg, j);
+                        const float su = __shfl_sync(0xffffffffu, fu, j);
+                        acc[j] = fmaf(__uint_as_float(r[j]), sg, acc[j]);
+                        acc[32 + j] = fmaf(__uint_as_float(r[32 + j]), su, acc[32 + j]);
+                    }
+                } else {
+                    uint32_t r[32];
+                    tmem_ld32(tcol, r);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float sg = __shfl_sync(0xffffffffu, fg, j);
+                        acc[j] = fmaf(__uint_as_float(r[j]), sg, acc[j]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[buf]));
+                if (++buf == C::NBUF) {
+                    buf = 0;
+                    tphase ^= 1u;
+                }
+                a0 = a1; g0 = g1; u0 = u1;
+                a1 = a2; g1 = g2; u1 = u2;
+            }
+            if (!ok) break;
+
+            if (GATED) {
+                // h = silu(g) * u; group amax over the 128 features of each token
+                float my_max = 0.f;  // lane j ends with this warp's max for token j
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float g = acc[j], u = acc[32 + j];
+                    const float h = nvalid ? __fdividef(g, 1.0f + __expf(-g)) * u : 0.f;
+                    acc[j] = h;
+                    float m = fabsf(h);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    if (lane == j) my_max = m;
+                }
+                s_amax[tpar][quarter][lane] = my_max;
+                mbar_arrive(smem_u32(&amax_bar));
+                if (!mbar_wait(smem_u32(&amax_bar), tpar, abort_p, err, kErrTimeoutEpilogue)) break;
+                const float amax = fmaxf(fmaxf(s_amax[tpar][0][lane], s_amax[tpar][1][lane]),
+                                         fmaxf(s_amax[tpar][2][lane], s_amax[tpar][3][lane]));
+                const float s_tok = group_scale(amax);  // lane j: scale of token j
+                if (quarter == 0 && lane < ti.rows) p.sh[(size_t)ti.nt * p.R + ti.row0 + lane] = s_tok;
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    const float s0 = __shfl_sync(0xffffffffu, s_tok, j);
+                    const float s1 = __shfl_sync(0xffffffffu, s_tok, j + 1);
+                    const uint32_t codes = e4m3x2(__fdiv_rn(acc[j], s0), __fdiv_rn(acc[j + 1], s1));
+                    if (j < ti.rows) p.hq[(size_t)(ti.row0 + j) * p.ldq + n] = (uint8_t)(codes & 0xffu);
+                    if (j + 1 < ti.rows) p.hq[(size_t)(ti.row0 + j + 1) * p.ldq + n] = (uint8_t)(codes >> 8);
+                }
+            } else {
+                const int slot_l = __ldg(p.perm + min(ti.row0 + lane, p.R - 1));
+                const float w_l = bf16_bits_to_f32(__ldg(p.topk_wb + slot_l));
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int slot = __shfl_sync(0xffffffffu, slot_l, j);
+                    const float w = __shfl_sync(0xffffffffu, w_l, j);
+                    if (j < ti.rows) p.part[(size_t)slot * p.ldp + n] = w * acc[j];
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+template <bool GATED>
+static cudaError_t launch_dec(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int grid,
+                              cudaStream_t st) {
+    using C = DecCfg<GATED>;
+    cudaError_t e = cudaFuncSetAttribute(moe_gemm_decode_kernel<GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(moe_gemm_decode_kernel<GATED>, dim3(grid), dim3(C::THREADS), (size_t)C::SMEM_BYTES, st, tmW,
+                      tmX, p);
+}
+
+cudaError_t launch_gemm_gateup_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int grid,
+                                      cudaStream_t st) {
+    return launch_dec<true>(tmW, tmX, p, grid, st);
+}
+
+cudaError_t launch_gemm_down_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int grid,
+                                    cudaStream_t st) {
+    return launch_dec<false>(tmW, tmX, p, grid, st);
+}
+
+}  // namespace moe

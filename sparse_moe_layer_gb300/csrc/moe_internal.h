@@ -15,7 +15,8 @@ struct RouteParams {
     const uint16_t* rb;  // bf16 [E]
     int T, H, E, k;
     int nchunks;  // ceil(T / kChunkTokens)
-    int nt1, nt2; // n-tiles per 128-row M tile: gate/up GEMM (Ip/128), down GEMM (Hp/128)
+    int nt1, nt2; // n-tiles per M tile: gate/up GEMM (Ip/128), down GEMM (Hp/128)
+    int bm;       // rows per M tile: 128 (prefill kernels) or 32 (decode kernels)
     int32_t* topk_idx;
     float* topk_w;
     uint16_t* topk_wb;
@@ -39,8 +40,9 @@ struct PermuteParams {
     const int32_t* chunk_base;
     int32_t* perm;
     int32_t* inv;
+    int R;        // T * k
     uint8_t* xq;  // [R, Hp]
-    float* sx;    // [R, Hp/128]
+    float* sx;    // [Hp/128, R] (K-block-major)
 };
 
 struct GemmParams {
@@ -52,11 +54,11 @@ struct GemmParams {
     const int32_t* count;
     const int32_t* offset;
     const int32_t* tiles;  // [E+1] first tile of each expert
-    const float* sa;       // activation scales [R, KB]
+    const float* sa;       // activation scales [KB, R] (K-block-major)
     const float* sw;       // weight scales [E, rows_B/128, KB]
     const uint16_t* bias;  // gate/up: b13 [E, 2I]; down: b2 [E, H]
     uint8_t* hq;           // gate/up output codes [R, ldq]
-    float* sh;             // gate/up output scales [R, ldq/128]
+    float* sh;             // gate/up output scales [ldq/128, R] (K-block-major)
     int ldq;
     const int32_t* perm;      // down: row -> t*k + j
     const uint16_t* topk_wb;  // down: routing weights bf16 [T*k]
@@ -96,5 +98,9 @@ cudaError_t launch_gemm_gateup(const CUtensorMap& tmA, const CUtensorMap& tmB, c
                                cudaStream_t st);
 cudaError_t launch_gemm_down(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
                              cudaStream_t st);
+cudaError_t launch_gemm_gateup_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int grid,
+                                      cudaStream_t st);
+cudaError_t launch_gemm_down_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int grid,
+                                    cudaStream_t st);
 
 }  // namespace moe

@@ -106,7 +106,7 @@ __device__ void finish_scan(const RouteParams& p) {
             s_off[e] = off;
             p.offset[e] = off;
             p.count[e] = c;
-            const int mt = (c + 127) / 128;
+            const int mt = (c + p.bm - 1) / p.bm;
             p.tiles1[e] = t1;
             p.tiles2[e] = t2;
             off += c;
@@ -118,6 +118,7 @@ __device__ void finish_scan(const RouteParams& p) {
         p.tiles2[p.E] = t2;
         p.status[kStatusTiles1] = (uint32_t)t1;
         p.status[kStatusTiles2] = (uint32_t)t2;
+        p.status[kStatusTileRows] = (uint32_t)p.bm;
     }
     __syncthreads();
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
@@ -406,7 +407,7 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
         for (int j = 0; j < p.k; ++j) {
             const int r = s_row[tt * p.k + j];
             *reinterpret_cast<uint32_t*>(p.xq + (size_t)r * p.Hp + c) = q;
-            if (lane == 0) p.sx[(size_t)r * G + g] = s;
+            if (lane == 0) p.sx[(size_t)g * p.R + r] = s;  // K-block-major [Hp/128, R]
         }
     }
 }
@@ -467,7 +468,9 @@ cudaError_t launch_combine(const float* part, int T, int H, int ldp, int k, uint
 }
 
 // ============================================================ weight packer
-// One CTA per (128x128 destination block, expert).  Destination row dr maps
+// One CTA per (128x128 destination block, expert); blocks are stored
+// contiguously (16 KB each, [E][row block][K block][128][128]) so the GEMMs
+// stream every weight tile as one contiguous 16 KB read.  Destination row dr maps
 // to a source row: gated_I > 0 (w13): gate rows [0,I) -> [0,I), up rows
 // [I,2I) -> [Ip, Ip+I); gated_I == 0 (w2): identity.  Rows/columns beyond
 // the source are zero pad.  s = amax/448 (1 for an all-zero block), code =
@@ -505,7 +508,9 @@ __global__ void __launch_bounds__(256) pack_blocks_kernel(const float* __restric
     uint32_t packed[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) packed[i] = quant4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], sc);
-    uint4* dst = reinterpret_cast<uint4*>(q + ((size_t)e * rows_p + dr) * cols_p + c0);
+    // blocked layout: block (e, bi, bj) is 16 KB contiguous, row-major inside
+    const size_t blk = ((size_t)e * (rows_p / 128) + bi) * (cols_p / 128) + bj;
+    uint4* dst = reinterpret_cast<uint4*>(q + blk * 16384 + (size_t)r_local * 128 + (threadIdx.x & 1) * 64);
 #pragma unroll
     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
     if (threadIdx.x == 0) s[((size_t)e * (rows_p / 128) + bi) * (cols_p / 128) + bj] = sc;

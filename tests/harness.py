@@ -73,9 +73,9 @@ class Layer:
         self.d_rb = bf16_np_to_torch(self.rb)
         self.d_b13 = bf16_np_to_torch(self.b13)
         self.d_b2 = bf16_np_to_torch(self.b2)
-        self.d_w13 = torch.empty((E, 2 * Ip, Hp), dtype=torch.uint8, device=dev)
+        self.d_w13 = torch.empty(moe.w13_shape(E, H, I), dtype=torch.uint8, device=dev)
         self.d_s13 = torch.empty((E, 2 * Ip // 128, Hp // 128), dtype=torch.float32, device=dev)
-        self.d_w2 = torch.empty((E, Hp, Ip), dtype=torch.uint8, device=dev)
+        self.d_w2 = torch.empty(moe.w2_shape(E, H, I), dtype=torch.uint8, device=dev)
         self.d_s2 = torch.empty((E, Hp // 128, Ip // 128), dtype=torch.float32, device=dev)
         for e0 in range(0, E, chunk_experts):
             n = min(chunk_experts, E - e0)

@@ -60,8 +60,10 @@ def full_check(moe, layer: Layer, n_sample: int | None = None):
     for key in ("count", "offset", "perm", "inv"):
         assert np.array_equal(v[key].cpu().numpy(), p[key]), key
     # GEMM tile lists cover every expert's rows
-    mt = (p["count"] + 127) // 128
     st = v["status"].cpu().numpy()
+    bm = 32 if T * k <= 64 * E else 128  # decode-sized batches use 32-row token tiles
+    assert st[3] == bm
+    mt = (p["count"] + bm - 1) // bm
     assert st[1] == mt.sum() * (layer.Ip // 128) and st[2] == mt.sum() * (layer.Hp // 128)
     # x quantisation: bit-exact codes and scales in every permuted row
     xq, sx = oracle.quant_rows_bf16(layer.x)
@@ -105,8 +107,9 @@ def test_pack_weights_bit_exact(moe, H, I, E):
     q13, s13, q2, s2 = moe.pack_weights(torch.from_numpy(w13).cuda(), torch.from_numpy(w2).cuda())
     oq13, os13 = oracle.pack_w13(w13)
     oq2, os2 = oracle.pack_w2(w2)
-    assert np.array_equal(q13.cpu().numpy(), oq13) and np.array_equal(s13.cpu().numpy(), os13)
-    assert np.array_equal(q2.cpu().numpy(), oq2) and np.array_equal(s2.cpu().numpy(), os2)
+    # the library stores each 128x128 block contiguously; compare in row-major order
+    assert np.array_equal(moe.unblock(q13).cpu().numpy(), oq13) and np.array_equal(s13.cpu().numpy(), os13)
+    assert np.array_equal(moe.unblock(q2).cpu().numpy(), oq2) and np.array_equal(s2.cpu().numpy(), os2)
 
 
 def test_tiny_layer_all_tokens(moe):
