@@ -122,6 +122,33 @@ moe_status moe_forward_profiled(const void* x, const void* router_w, const void*
                                 size_t workspace_bytes, void* stream, void* const* events);
 
 /*
+ * moe_forward for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that may not call cudaMalloc/cudaFree themselves -- for example plugins
+ * whose device memory is owned by a host framework's caching allocator or a
+ * serving engine's fixed pool, or code that must keep allocation and the
+ * synchronisation cudaFree implies out of its latency path.  Same arguments
+ * and results as moe_forward, without the workspace: the library uses a
+ * file-scope device array of 32 MiB (MOE_STATIC_SCRATCH_BYTES) instead, which
+ * every GPU that loads the library holds until the process exits.
+ *   - Sizes whose moe_workspace_size exceeds 32 MiB are rejected with
+ *     MOE_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and it keeps the last
+ *     call's contents (each call clears what must start at zero itself).
+ *     Calls whose kernels overlap on the GPU (other streams, other host
+ *     threads) race on it; serialise them.
+ *   - Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define MOE_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+moe_status moe_forward_static_scratch(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
+                                      const float* s13, const void* b13, const uint8_t* w2, const float* s2,
+                                      const void* b2, int T, int H, int I, int E, int top_k, void* out, void* stream);
+
+/*
  * Weight packer (the offline converter from master weights to the layer's
  * FP8 layout; "GPT-OSS on Day 0": FP8 with 128x128 block scaling).
  *   w13_f32 fp32 [E, 2*I, H] (gate rows then up rows), w2_f32 fp32 [E, H, I]  (device)

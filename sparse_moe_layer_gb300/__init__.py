@@ -57,6 +57,8 @@ def lib():
         L.moe_forward.restype = i32
         L.moe_forward_profiled.argtypes = [vp] * 9 + [i32] * 5 + [vp, vp, sz, vp, vp]
         L.moe_forward_profiled.restype = i32
+        L.moe_forward_static_scratch.argtypes = [vp] * 9 + [i32] * 5 + [vp, vp]
+        L.moe_forward_static_scratch.restype = i32
         L.moe_pack_weights.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
         L.moe_pack_weights.restype = i32
         L.moe_quantize_rows.argtypes = [vp, i32, i32, i32, vp, vp, vp]

@@ -287,6 +287,54 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     return MOE_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Forward with a library-owned scratch area, for callers that cannot allocate.
+//
+// Some callers cannot call cudaMalloc: plugins whose device memory belongs to
+// a host framework's caching allocator or a serving engine's fixed memory
+// pool, and code that must keep cudaMalloc/cudaFree (and the synchronisation
+// cudaFree implies) out of its latency path.  For them the layer's scratch
+// lives in this file-scope device array: every GPU that loads the library
+// holds it until the process exits, and every call on a device shares it.
+// Host code must not pass g_static_scratch itself to a kernel -- in host code
+// that name is a host-side stand-in, not a device address -- so the device
+// address is looked up once per device with cudaGetSymbolAddress.
+constexpr size_t kStaticScratchBytes = (size_t)32 << 20;  // 32 MiB
+__device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" moe_status moe_forward_static_scratch(const void* x, const void* router_w, const void* router_b,
+                                                 const uint8_t* w13, const float* s13, const void* b13,
+                                                 const uint8_t* w2, const float* s2, const void* b2, int T, int H,
+                                                 int I, int E, int top_k, void* out, void* stream) {
+    const size_t need = moe_workspace_size(T, H, I, E, top_k);
+    if (need == 0) return MOE_ERR_INVALID_ARG;
+    if (need > kStaticScratchBytes) return MOE_ERR_WORKSPACE;  // these sizes need more than the static area
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        if (!g_scratch_addr[dev]) {
+            // first call on this device (which is current): find the array's device address
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+            g_scratch_addr[dev] = p;
+        }
+        scratch = g_scratch_addr[dev];
+    }
+    // forward_impl clears the status words and the expert histogram at the
+    // start of every call, so nothing left by the previous call leaks in.
+    return forward_impl(x, router_w, router_b, w13, s13, b13, w2, s2, b2, T, H, I, E, top_k, out, scratch,
+                        kStaticScratchBytes, stream, nullptr);
+}
+
 extern "C" {
 
 moe_status moe_pack_weights(const float* w13_f32, const float* w2_f32, int H, int I, int E, uint8_t* w13, float* s13,
