@@ -33,11 +33,46 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo_val, float hi_val) {
 // fp32, 1 for an all-zero group (its codes are then all +0).
 __device__ __forceinline__ float group_scale(float amax) { return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f); }
 
-// Four values of one group -> four e4m3 codes (byte i = value i), v/s in IEEE fp32.
-__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float s) {
-    uint32_t lo = e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s));
-    uint32_t hi = e4m3x2(__fdiv_rn(c, s), __fdiv_rn(d, s));
+// The correctly rounded fp32 quotient v/s, given r = RN(1/s): q0 = RN(v*r),
+// rem = v - q0*s (exact with one FMA), q = RN(q0 + rem*r) -- Markstein's
+// correction step (P. Markstein, "Computation of elementary functions on the
+// IBM RISC System/6000 processor", IBM J. Res. Dev. 1990).  The remainder is
+// exact only while it stays in the normal range, so the step is taken for
+// |v| >= 2^-96 (then s >= |v|/448 is normal as well); zeros (whose sign the
+// step would lose), tiny values and NaN take IEEE division.  Checked
+// bit-for-bit against IEEE division by the quantiser tests.
+__device__ __forceinline__ float recip_rn(float s) { return __frcp_rn(s); }
+__device__ __forceinline__ float div_by(float v, float s, float r) {
+    if (!(fabsf(v) >= 0x1p-96f)) return __fdiv_rn(v, s);
+    const float q0 = __fmul_rn(v, r);
+    const float rem = __fmaf_rn(-q0, s, v);
+    return __fmaf_rn(rem, r, q0);
+}
+
+// Four values of one group -> four e4m3 codes (byte i = value i): e4m3(v/s),
+// v/s correctly rounded in fp32 (r = recip_rn(s)).
+__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float s, float r) {
+    uint32_t lo = e4m3x2(div_by(a, s, r), div_by(b, s, r));
+    uint32_t hi = e4m3x2(div_by(c, s, r), div_by(d, s, r));
     return lo | (hi << 16);
+}
+
+// Max over the 32 lanes of column j of v (each lane holds one row of 32
+// values), returned in lane j: a transpose-and-reduce butterfly that halves
+// the columns a lane keeps at every step (31 shuffles instead of 32 x 5).
+// v is overwritten.
+__device__ __forceinline__ float column_max32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int n = 16; n >= 1; n >>= 1) {
+        const bool hi = (lane & n) != 0;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+            const float send = hi ? v[i] : v[i + n];
+            const float keep = hi ? v[i + n] : v[i];
+            v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, n));
+        }
+    }
+    return v[0];
 }
 
 // ------------------------------------------------------------- smem/ptx ----

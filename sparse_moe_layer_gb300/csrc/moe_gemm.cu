@@ -94,10 +94,12 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
     __shared__ __align__(8) uint64_t tempty_bar[C::NBUF][C::HALVES];
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ __align__(8) uint64_t amax_bar;  // gate/up epilogue: the two column halves of a row meet here
+    __shared__ __align__(8) uint64_t bias_bar;  // the staged bias of a tile is complete
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ int s_tiles[kMaxExperts + 1], s_off[kMaxExperts + 1], s_cnt[kMaxExperts];
     __shared__ float s_amax[2][2][128];  // [tile parity][column half][row]
+    __shared__ float s_bias[2][C::BN];   // [tile parity][tile column]: bias of the tile, staged one tile ahead
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = p.E;
@@ -113,6 +115,7 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             }
         mbar_init(smem_u32(&drain_bar), 1);
         mbar_init(smem_u32(&amax_bar), C::EPI_WARPS * 32);
+        mbar_init(smem_u32(&bias_bar), C::EPI_WARPS * 32);
         abort_flag = 0;
         fence_barrier_init();
     }
@@ -255,39 +258,68 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
         uint32_t tphase = 0;
         uint32_t tpar = 0;  // parity of the tiles this CTA has finished
         bool ok = true;
+        const int up_off = GATED ? (p.up_rows / 128) * p.KB : 0;  // sw_u = sw_g + up_off
+        // The bias of a tile goes to shared memory (one value per epilogue
+        // thread) and the scales of its first two K blocks to registers while
+        // the previous tile's epilogue still runs, so a new tile never starts
+        // with a wait on global memory.
+        auto stage_bias = [&](const TileInfo& t, int slot) {
+            const int c = ew * 32 + lane;  // 0..255: tile column (gate: [0,128), up: [128,256))
+            if (c < C::BN) {
+                const int hh = c >> 7, n = t.nt * 128 + (c & 127);
+                const uint16_t* bias_e = p.bias + (size_t)t.e * (GATED ? 2 * p.N_real : p.N_real);
+                s_bias[slot][c] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + hh * p.N_real + n)) : 0.f;
+            }
+        };
+        struct Pre {
+            float a0, g0, u0, a1, g1, u1;
+        };
+        auto load_scales = [&](const TileInfo& t) {
+            Pre q{0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const int gr = min(t.row0 + row, p.R - 1);
+            const float* sw = p.sw + ((size_t)t.e * p.sw_rowblocks + t.nt) * p.KB;
+            q.a0 = __ldg(p.sa + gr);
+            q.g0 = __ldg(sw);
+            if (GATED) q.u0 = __ldg(sw + up_off);
+            if (p.KB > 1) {
+                q.a1 = __ldg(p.sa + (size_t)p.R + gr);
+                q.g1 = __ldg(sw + 1);
+                if (GATED) q.u1 = __ldg(sw + up_off + 1);
+            }
+            return q;
+        };
+        TileInfo nxt{};
+        Pre pre{0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (blockIdx.x < total) {
+            nxt = decode_tile(blockIdx.x, s_tiles, s_off, s_cnt, E);
+            stage_bias(nxt, 0);
+            pre = load_scales(nxt);
+        }
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, tpar ^= 1u) {
-            const TileInfo ti = decode_tile(tile, s_tiles, s_off, s_cnt, E);
+            const TileInfo ti = nxt;
             const int grow = ti.row0 + row;
             const bool valid = row < ti.rows;
             const int grow_c = min(grow, p.R - 1);
             float acc[C::COLS];
-            const uint16_t* bias_e = p.bias + (size_t)ti.e * (GATED ? 2 * p.N_real : p.N_real);
             const int n0 = ti.nt * 128 + 64 * half;
+            // the staged bias is visible once all epilogue warps passed the previous
+            // tile's amax barrier (gate/up) or this tile's first buffer hand-over
+            // ordering; a bounded barrier among the epilogue warps makes it explicit
+            mbar_arrive(smem_u32(&bias_bar));
+            if (!mbar_wait(smem_u32(&bias_bar), tpar, abort_p, err, kErrTimeoutEpilogue)) break;
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
-                const int n = n0 + i;
-                acc[i] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + n)) : 0.f;
-                if (GATED) acc[64 + i] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + p.N_real + n)) : 0.f;
+                acc[i] = s_bias[tpar][64 * half + i];
+                if (GATED) acc[64 + i] = s_bias[tpar][128 + 64 * half + i];
             }
             const float* sa_row = p.sa + grow_c;  // element kb at sa_row[kb * R]
             const float* sw_g = p.sw + ((size_t)ti.e * p.sw_rowblocks + ti.nt) * p.KB;
-            const int up_off = GATED ? (p.up_rows / 128) * p.KB : 0;  // sw_u = sw_g + up_off
             // Warps whose TMEM lane quarter holds no valid row of this tile only
             // keep the buffer hand-over going (decode tiles have few rows).
             const bool active = quarter * 32 < ti.rows;
             // scales of K blocks kb and kb+1 are in registers; kb+2 is loaded
             // while kb is promoted, so no K block waits on a global load
-            float a0 = 0.f, g0 = 0.f, u0 = 0.f, a1 = 0.f, g1 = 0.f, u1 = 0.f;
-            if (active) {
-                a0 = __ldg(sa_row);
-                g0 = __ldg(sw_g);
-                if (GATED) u0 = __ldg(sw_g + up_off);
-                if (p.KB > 1) {
-                    a1 = __ldg(sa_row + (size_t)p.R);
-                    g1 = __ldg(sw_g + 1);
-                    if (GATED) u1 = __ldg(sw_g + up_off + 1);
-                }
-            }
+            float a0 = pre.a0, g0 = pre.g0, u0 = pre.u0, a1 = pre.a1, g1 = pre.g1, u1 = pre.u1;
             for (int kb = 0; kb < p.KB; ++kb) {
                 float a2 = 0.f, g2 = 0.f, u2 = 0.f;
                 if (active && kb + 2 < p.KB) {
@@ -326,6 +358,11 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 a1 = a2; g1 = g2; u1 = u2;
             }
             if (!ok) break;
+            if (tile + (int)gridDim.x < total) {
+                nxt = decode_tile(tile + gridDim.x, s_tiles, s_off, s_cnt, E);
+                stage_bias(nxt, tpar ^ 1u);
+                pre = load_scales(nxt);
+            }
 
             if (GATED) {
                 // h = silu(g) * u for this thread's 64 columns of the 128-wide group
@@ -345,6 +382,7 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 if (!mbar_wait(smem_u32(&amax_bar), tpar, abort_p, err, kErrTimeoutEpilogue)) break;
                 amax = fmaxf(s_amax[tpar][0][row], s_amax[tpar][1][row]);
                 const float s = group_scale(amax);
+                const float rs = recip_rn(s);
                 if (valid) {
                     uint4* dst = reinterpret_cast<uint4*>(p.hq + (size_t)grow * p.ldq + ti.nt * 128 + 64 * half);
 #pragma unroll
@@ -353,7 +391,7 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const int i = 16 * v + 4 * q;
-                            w[q] = quant4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3], s);
+                            w[q] = quant4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3], s, rs);
                         }
                         dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
                     }

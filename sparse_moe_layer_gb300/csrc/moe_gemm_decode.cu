@@ -18,8 +18,13 @@
 //   warp 1     TMEM allocator and MMA issuer
 //   warps 2-5  promotion + epilogue, one TMEM lane quarter (32 features) each:
 //              gate/up: h = silu(g)*u, 1x128 requant across the 128 features of
-//              a token (warp shuffles + shared memory), codes -> hq, scales -> sh
-//              down: * routing weight -> part[t*k+j, n]
+//              a token (column max by shuffles + shared memory), codes -> hq,
+//              scales -> sh;  down: * routing weight -> part[t*k+j, n]
+//   warp 6     metadata: stages each tile's bias, token scales, weight scales
+//              (and, for the down GEMM, the tokens' slots and routing weights)
+//              in shared memory one tile ahead, so neither the promotion nor
+//              the epilogue waits on global memory and a tile's epilogue is
+//              short enough for the MMA to run on into the next tile.
 #include <cuda_bf16.h>
 
 #include "moe_device.cuh"
@@ -33,13 +38,23 @@ struct DecCfg {
     static constexpr int W_BYTES = (GATED ? 2 : 1) * 128 * 128;
     static constexpr int X_BYTES = BT * 128;
     static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
-    static constexpr int STAGES = GATED ? 5 : 10;
+    static constexpr int STAGES = GATED ? 5 : 9;
     static constexpr int ACC_COLS = GATED ? 2 * BT : BT;  // TMEM columns of one accumulation buffer
-    static constexpr int TMEM_COLS = 256;
-    static constexpr int NBUF = TMEM_COLS / ACC_COLS;     // 4 (gate/up) or 8 (down)
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int NBUF = TMEM_COLS / ACC_COLS;     // 8 (gate/up) or 16 (down)
     static constexpr int EPI_WARPS = 4;
-    static constexpr int THREADS = (2 + EPI_WARPS) * 32;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+    static constexpr int META_WARP = 6;
+    static constexpr int THREADS = 7 * 32;
+    static constexpr int KB_MAX = 128;                    // K <= 16384
+    // one metadata slot (floats): bias [256], token scales [KB_MAX][32], weight scales [2][KB_MAX],
+    // token slots [32] (int) and routing weights [32]
+    static constexpr int M_BIAS = 0;
+    static constexpr int M_SA = 256;
+    static constexpr int M_SW = M_SA + KB_MAX * 32;
+    static constexpr int M_SLOT = M_SW + 2 * KB_MAX;
+    static constexpr int M_W = M_SLOT + 32;
+    static constexpr int META_FLOATS = M_W + 32;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 2 * META_FLOATS * 4 + 1024;
     static constexpr uint32_t IDESC = idesc_e4m3_f32(128, BT);
 };
 
@@ -75,11 +90,14 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
     using C = DecCfg<GATED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    float* meta = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES);  // [2][META_FLOATS]
 
     __shared__ __align__(8) uint64_t full_bar[C::STAGES];
     __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
     __shared__ __align__(8) uint64_t tfull_bar[C::NBUF];
     __shared__ __align__(8) uint64_t tempty_bar[C::NBUF];
+    __shared__ __align__(8) uint64_t mfull_bar[2];
+    __shared__ __align__(8) uint64_t mempty_bar[2];
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ __align__(8) uint64_t amax_bar;
     __shared__ uint32_t tmem_slot;
@@ -97,6 +115,10 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
         for (int b = 0; b < C::NBUF; ++b) {
             mbar_init(smem_u32(&tfull_bar[b]), 1);
             mbar_init(smem_u32(&tempty_bar[b]), C::EPI_WARPS);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&mfull_bar[b]), 32);
+            mbar_init(smem_u32(&mempty_bar[b]), C::EPI_WARPS * 32);
         }
         mbar_init(smem_u32(&drain_bar), 1);
         mbar_init(smem_u32(&amax_bar), C::EPI_WARPS * 32);
@@ -209,57 +231,73 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
             int dummy = 0;
             mbar_wait(smem_u32(&drain_bar), 0, &dummy, err, kErrTimeoutMma);
         }
-    } else {
+    } else if (warp == C::META_WARP) {
+        // --------------------------------------------------- metadata warp
+        int it = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+            const int slot = it & 1;
+            const uint32_t use = (uint32_t)(it >> 1) & 1u;  // parity of this slot's use
+            if (!mbar_wait(smem_u32(&mempty_bar[slot]), use ^ 1u, abort_p, err, kErrTimeoutProducer)) break;
+            float* m = meta + slot * C::META_FLOATS;
+            const DecTile ti = decode_dec_tile(tile, s_tiles, s_off, s_cnt, E);
+            const uint16_t* bias_e = p.bias + (size_t)ti.e * (GATED ? 2 * p.N_real : p.N_real);
+#pragma unroll
+            for (int c = lane; c < (GATED ? 256 : 128); c += 32) {
+                const int n = ti.nt * 128 + (c & 127);
+                m[C::M_BIAS + c] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + (c >> 7) * p.N_real + n)) : 0.f;
+            }
+            const int rtok = min(ti.row0 + lane, p.R - 1);
+            for (int kb = 0; kb < p.KB; ++kb) m[C::M_SA + kb * 32 + lane] = __ldg(p.sa + (size_t)kb * p.R + rtok);
+            const float* sw_g = p.sw + ((size_t)ti.e * p.sw_rowblocks + ti.nt) * p.KB;
+            for (int kb = lane; kb < p.KB; kb += 32) {
+                m[C::M_SW + kb] = __ldg(sw_g + kb);
+                if (GATED) m[C::M_SW + C::KB_MAX + kb] = __ldg(sw_g + (p.up_rows / 128) * p.KB + kb);
+            }
+            if (!GATED) {
+                const int slot_t = __ldg(p.perm + rtok);
+                reinterpret_cast<int*>(m)[C::M_SLOT + lane] = slot_t;
+                m[C::M_W + lane] = bf16_bits_to_f32(__ldg(p.topk_wb + slot_t));
+            }
+            mbar_arrive(smem_u32(&mfull_bar[slot]));
+        }
+    } else if (warp >= 2 && warp < 2 + C::EPI_WARPS) {
         // -------------------------------------------- promotion + epilogue
         const int quarter = warp & 3;            // TMEM lanes this warp may access
         const int nl = quarter * 32 + lane;      // output feature within the 128-wide n-tile
         const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
-        int buf = 0;
-        uint32_t tphase = 0, tpar = 0;
+        int buf = 0, it = 0;
+        uint32_t tphase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, tpar ^= 1u) {
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+            const int slot = it & 1;
+            const uint32_t use = (uint32_t)(it >> 1) & 1u;
+            const uint32_t tpar = (uint32_t)it & 1u;
+            if (!mbar_wait(smem_u32(&mfull_bar[slot]), use, abort_p, err, kErrTimeoutEpilogue)) break;
+            const float* m = meta + slot * C::META_FLOATS;
             const DecTile ti = decode_dec_tile(tile, s_tiles, s_off, s_cnt, E);
             const int n = ti.nt * 128 + nl;
             const bool nvalid = n < p.N_real;
             float acc[C::ACC_COLS];
             {
-                const uint16_t* bias_e = p.bias + (size_t)ti.e * (GATED ? 2 * p.N_real : p.N_real);
-                const float bg = nvalid ? bf16_bits_to_f32(__ldg(bias_e + n)) : 0.f;
-                const float bu = (GATED && nvalid) ? bf16_bits_to_f32(__ldg(bias_e + p.N_real + n)) : 0.f;
+                const float bg = m[C::M_BIAS + nl];
+                const float bu = GATED ? m[C::M_BIAS + 128 + nl] : 0.f;
 #pragma unroll
                 for (int j = 0; j < C::BT; ++j) {
                     acc[j] = bg;
                     if (GATED) acc[C::BT + j] = bu;
                 }
             }
-            // this lane's token: scales of K blocks kb, kb+1 in registers, kb+2 loading
-            const int rtok = min(ti.row0 + lane, p.R - 1);
-            const float* sa_col = p.sa + rtok;  // element kb at sa_col[kb * R]
-            const float* sw_g = p.sw + ((size_t)ti.e * p.sw_rowblocks + ti.nt) * p.KB;
-            const int up_off = GATED ? (p.up_rows / 128) * p.KB : 0;
-            float a0 = __ldg(sa_col), g0 = __ldg(sw_g), u0 = GATED ? __ldg(sw_g + up_off) : 0.f;
-            float a1 = 0.f, g1 = 0.f, u1 = 0.f;
-            if (p.KB > 1) {
-                a1 = __ldg(sa_col + (size_t)p.R);
-                g1 = __ldg(sw_g + 1);
-                if (GATED) u1 = __ldg(sw_g + up_off + 1);
-            }
             for (int kb = 0; kb < p.KB; ++kb) {
-                float a2 = 0.f, g2 = 0.f, u2 = 0.f;
-                if (kb + 2 < p.KB) {
-                    a2 = __ldg(sa_col + (size_t)(kb + 2) * p.R);
-                    g2 = __ldg(sw_g + kb + 2);
-                    if (GATED) u2 = __ldg(sw_g + up_off + kb + 2);
-                }
                 if (!mbar_wait(smem_u32(&tfull_bar[buf]), tphase, abort_p, err, kErrTimeoutEpilogue)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t tcol = t_lane + (uint32_t)(buf * C::ACC_COLS);
-                const float fg = a0 * g0;  // lane j: scale of token j for the gate (or down) rows
-                const float fu = a0 * u0;
+                const float a = m[C::M_SA + kb * 32 + lane];  // lane j: scale of token j in this K block
+                const float fg = a * m[C::M_SW + kb];
                 if (GATED) {
+                    const float fu = a * m[C::M_SW + C::KB_MAX + kb];
                     uint32_t r[64];
                     tmem_ld64(tcol, r);
 #pragma unroll
@@ -285,47 +323,47 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                     buf = 0;
                     tphase ^= 1u;
                 }
-                a0 = a1; g0 = g1; u0 = u1;
-                a1 = a2; g1 = g2; u1 = u2;
             }
             if (!ok) break;
 
             if (GATED) {
-                // h = silu(g) * u; group amax over the 128 features of each token
-                float my_max = 0.f;  // lane j ends with this warp's max for token j
+                mbar_arrive(smem_u32(&mempty_bar[slot]));  // this tile's metadata is no longer read
+                // h = silu(g) * u; per-token amax over the 128 features (4 warps x 32 lanes)
+                float habs[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const float g = acc[j], u = acc[32 + j];
                     const float h = nvalid ? __fdividef(g, 1.0f + __expf(-g)) * u : 0.f;
                     acc[j] = h;
-                    float m = fabsf(h);
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                    if (lane == j) my_max = m;
+                    habs[j] = fabsf(h);
                 }
-                s_amax[tpar][quarter][lane] = my_max;
+                s_amax[tpar][quarter][lane] = column_max32(habs, lane);  // lane j: this warp's max for token j
                 mbar_arrive(smem_u32(&amax_bar));
                 if (!mbar_wait(smem_u32(&amax_bar), tpar, abort_p, err, kErrTimeoutEpilogue)) break;
                 const float amax = fmaxf(fmaxf(s_amax[tpar][0][lane], s_amax[tpar][1][lane]),
                                          fmaxf(s_amax[tpar][2][lane], s_amax[tpar][3][lane]));
                 const float s_tok = group_scale(amax);  // lane j: scale of token j
+                const float r_tok = recip_rn(s_tok);
                 if (quarter == 0 && lane < ti.rows) p.sh[(size_t)ti.nt * p.R + ti.row0 + lane] = s_tok;
 #pragma unroll
                 for (int j = 0; j < 32; j += 2) {
                     const float s0 = __shfl_sync(0xffffffffu, s_tok, j);
                     const float s1 = __shfl_sync(0xffffffffu, s_tok, j + 1);
-                    const uint32_t codes = e4m3x2(__fdiv_rn(acc[j], s0), __fdiv_rn(acc[j + 1], s1));
+                    const float r0 = __shfl_sync(0xffffffffu, r_tok, j);
+                    const float r1 = __shfl_sync(0xffffffffu, r_tok, j + 1);
+                    const uint32_t codes = e4m3x2(div_by(acc[j], s0, r0), div_by(acc[j + 1], s1, r1));
                     if (j < ti.rows) p.hq[(size_t)(ti.row0 + j) * p.ldq + n] = (uint8_t)(codes & 0xffu);
                     if (j + 1 < ti.rows) p.hq[(size_t)(ti.row0 + j + 1) * p.ldq + n] = (uint8_t)(codes >> 8);
                 }
             } else {
-                const int slot_l = __ldg(p.perm + min(ti.row0 + lane, p.R - 1));
-                const float w_l = bf16_bits_to_f32(__ldg(p.topk_wb + slot_l));
+                const int slot_l = reinterpret_cast<const int*>(m)[C::M_SLOT + lane];
+                const float w_l = m[C::M_W + lane];
+                mbar_arrive(smem_u32(&mempty_bar[slot]));
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const int slot = __shfl_sync(0xffffffffu, slot_l, j);
+                    const int slot_t = __shfl_sync(0xffffffffu, slot_l, j);
                     const float w = __shfl_sync(0xffffffffu, w_l, j);
-                    if (j < ti.rows) p.part[(size_t)slot * p.ldp + n] = w * acc[j];
+                    if (j < ti.rows) p.part[(size_t)slot_t * p.ldp + n] = w * acc[j];
                 }
             }
         }

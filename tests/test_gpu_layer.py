@@ -92,9 +92,14 @@ def test_quantize_rows_bit_exact(moe):
     v[3] = 0.0
     v[5, 128:256] = 0.0
     v[6, :7] = np.float32([448.0, -448.0, 1e-30, -1e-30, 2.0 ** -9, 3.0, -0.0])
+    v[7, :5] = np.float32([-0.0, 1e-39, -1e-39, 2.0 ** -100, -(2.0 ** -110)])  # signed zero, subnormals, tiny
+    v[8, :128] = np.float32(2.0 ** -120) * np.linspace(-1, 1, 128, dtype=np.float32)  # a whole group of tiny values
     q, s = moe.quantize_rows(torch.from_numpy(v).cuda())
     qo, so = oracle.quant_rows_f32(v)
-    assert np.array_equal(q.cpu().numpy(), qo)
+    qg = q.cpu().numpy()
+    bad = np.argwhere(qg != qo)
+    assert len(bad) == 0, [(int(r), int(c), float(v[r, c]) if c < v.shape[1] else None, int(qg[r, c]), int(qo[r, c]))
+                           for r, c in bad[:8]]
     assert np.array_equal(s.cpu().numpy(), so)
 
 
