@@ -208,9 +208,21 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     pp.Hp = Hp;
     pp.E = E;
     pp.k = top_k;
-    pp.tokens_per_cta = T <= 2048 ? 1 : 8;
+    // 8 tokens per CTA for large batches while their x rows fit in 96 KB of shared memory
+    pp.tokens_per_cta = (T > 2048 && 8LL * ((H + 7) & ~7) * 2 <= 96 * 1024) ? 8 : 1;
     pp.topk_idx = rp.topk_idx;
     pp.chunk_base = rp.chunk_base;
+    pp.scan_here = router_uses_mma(T, H) ? 0 : 1;
+    pp.nchunks = nch;
+    pp.bm = rp.bm;
+    pp.nt1 = rp.nt1;
+    pp.nt2 = rp.nt2;
+    pp.hist = rp.hist;
+    pp.count = rp.count;
+    pp.offset = rp.offset;
+    pp.tiles1 = rp.tiles1;
+    pp.tiles2 = rp.tiles2;
+    pp.status = rp.status;
     pp.perm = reinterpret_cast<int32_t*>(ws + L.perm);
     pp.inv = reinterpret_cast<int32_t*>(ws + L.inv);
     pp.xq = ws + L.xq;

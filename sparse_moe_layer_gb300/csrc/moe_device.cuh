@@ -57,6 +57,31 @@ __device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, f
     return lo | (hi << 16);
 }
 
+// h[i] = silu(g[i]) * u[i] = g/(1+exp(-g)) * u for i < N, written over g;
+// h = 0 for i >= n_valid (padding features).  Returns max_i |h[i]|.  The work
+// is issued in independent batches of 16 with four partial maxima, so the two
+// special-function operations per element overlap instead of forming one
+// long dependent chain.
+template <int N>
+__device__ __forceinline__ float swiglu_inplace(float* g, const float* u, int n_valid) {
+    float m[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int b = 0; b < N; b += 16) {
+        float e[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) e[i] = __expf(-g[b + i]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) e[i] = __frcp_rn(1.0f + e[i]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float h = (b + i < n_valid) ? g[b + i] * e[i] * u[b + i] : 0.f;
+            g[b + i] = h;
+            m[i & 3] = fmaxf(m[i & 3], fabsf(h));
+        }
+    }
+    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
 // Max over the 32 lanes of column j of v (each lane holds one row of 32
 // values), returned in lane j: a transpose-and-reduce butterfly that halves
 // the columns a lane keeps at every step (31 shuffles instead of 32 x 5).

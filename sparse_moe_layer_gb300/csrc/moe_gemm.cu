@@ -18,7 +18,8 @@
 //               expert's weight rows) per K block into a STAGES-deep ring.
 //   warp 1      TMEM allocator and MMA issuer (one thread): 4 MMAs of K=32
 //               per K block into TMEM buffer kb % NBUF, then commits.
-//   warps 2-3   idle (they complete warpgroup 0, which gives registers away)
+//   warp 2      metadata: stages each tile's bias in shared memory one tile ahead
+//   warp 3      idle (warpgroup 0 gives registers to the promotion warpgroups)
 //   warps 4-11  promotion + epilogue: tcgen05.ld the partial, FMA with the
 //               two scales into registers, release the buffer; after the last
 //               K block run the fused epilogue:
@@ -94,12 +95,13 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
     __shared__ __align__(8) uint64_t tempty_bar[C::NBUF][C::HALVES];
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ __align__(8) uint64_t amax_bar;  // gate/up epilogue: the two column halves of a row meet here
-    __shared__ __align__(8) uint64_t bias_bar;  // the staged bias of a tile is complete
+    __shared__ __align__(8) uint64_t bfull_bar[2];   // bias slot filled by the metadata warp
+    __shared__ __align__(8) uint64_t bempty_bar[2];  // bias slot read by every epilogue thread
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ int s_tiles[kMaxExperts + 1], s_off[kMaxExperts + 1], s_cnt[kMaxExperts];
     __shared__ float s_amax[2][2][128];  // [tile parity][column half][row]
-    __shared__ float s_bias[2][C::BN];   // [tile parity][tile column]: bias of the tile, staged one tile ahead
+    __shared__ float s_bias[2][C::BN];   // [slot][tile column]: bias of a tile, staged ahead by the metadata warp
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = p.E;
@@ -115,7 +117,10 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             }
         mbar_init(smem_u32(&drain_bar), 1);
         mbar_init(smem_u32(&amax_bar), C::EPI_WARPS * 32);
-        mbar_init(smem_u32(&bias_bar), C::EPI_WARPS * 32);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bfull_bar[b]), 32);
+            mbar_init(smem_u32(&bempty_bar[b]), C::EPI_WARPS * 32);
+        }
         abort_flag = 0;
         fence_barrier_init();
     }
@@ -246,6 +251,23 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             int dummy = 0;
             mbar_wait(smem_u32(&drain_bar), 0, &dummy, err, kErrTimeoutMma);
         }
+    } else if (warp == 2) {
+        // ---------------------------------------------------- metadata warp
+        // Stages each tile's bias in shared memory one tile ahead, so the
+        // epilogue warps never start a tile with a wait on global memory.
+        int it = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+            const int slot = it & 1;
+            const uint32_t use = (uint32_t)(it >> 1) & 1u;
+            if (!mbar_wait(smem_u32(&bempty_bar[slot]), use ^ 1u, abort_p, err, kErrTimeoutProducer)) break;
+            const TileInfo t = decode_tile(tile, s_tiles, s_off, s_cnt, E);
+            const uint16_t* bias_e = p.bias + (size_t)t.e * (GATED ? 2 * p.N_real : p.N_real);
+            for (int c = lane; c < C::BN; c += 32) {
+                const int n = t.nt * 128 + (c & 127);
+                s_bias[slot][c] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + (c >> 7) * p.N_real + n)) : 0.f;
+            }
+            mbar_arrive(smem_u32(&bfull_bar[slot]));
+        }
     } else if (warp >= 4) {
         // -------------------------------------------- promotion + epilogue
         if (GATED) regs_acquire<C::EPI_REGS>();
@@ -259,24 +281,20 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
         uint32_t tpar = 0;  // parity of the tiles this CTA has finished
         bool ok = true;
         const int up_off = GATED ? (p.up_rows / 128) * p.KB : 0;  // sw_u = sw_g + up_off
-        // The bias of a tile goes to shared memory (one value per epilogue
-        // thread) and the scales of its first two K blocks to registers while
-        // the previous tile's epilogue still runs, so a new tile never starts
-        // with a wait on global memory.
-        auto stage_bias = [&](const TileInfo& t, int slot) {
-            const int c = ew * 32 + lane;  // 0..255: tile column (gate: [0,128), up: [128,256))
-            if (c < C::BN) {
-                const int hh = c >> 7, n = t.nt * 128 + (c & 127);
-                const uint16_t* bias_e = p.bias + (size_t)t.e * (GATED ? 2 * p.N_real : p.N_real);
-                s_bias[slot][c] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + hh * p.N_real + n)) : 0.f;
-            }
-        };
+        // The scales of a tile's first two K blocks are loaded into registers
+        // while the previous tile's epilogue still runs; its bias arrives in
+        // shared memory from the metadata warp.
         struct Pre {
-            float a0, g0, u0, a1, g1, u1;
+            float a0, g0, u0, a1, g1, u1, w;
+            int slot;
         };
         auto load_scales = [&](const TileInfo& t) {
-            Pre q{0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            Pre q{0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0};
             const int gr = min(t.row0 + row, p.R - 1);
+            if (!GATED) {  // the row's slot and routing weight, used by the epilogue
+                q.slot = __ldg(p.perm + gr);
+                q.w = bf16_bits_to_f32(__ldg(p.topk_wb + q.slot));
+            }
             const float* sw = p.sw + ((size_t)t.e * p.sw_rowblocks + t.nt) * p.KB;
             q.a0 = __ldg(p.sa + gr);
             q.g0 = __ldg(sw);
@@ -289,29 +307,30 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             return q;
         };
         TileInfo nxt{};
-        Pre pre{0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        Pre pre{0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0};
         if (blockIdx.x < total) {
             nxt = decode_tile(blockIdx.x, s_tiles, s_off, s_cnt, E);
-            stage_bias(nxt, 0);
             pre = load_scales(nxt);
         }
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, tpar ^= 1u) {
+        int tcount = 0;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, tpar ^= 1u, ++tcount) {
             const TileInfo ti = nxt;
+            const int my_slot = pre.slot;
+            const float my_w = pre.w;
             const int grow = ti.row0 + row;
             const bool valid = row < ti.rows;
             const int grow_c = min(grow, p.R - 1);
             float acc[C::COLS];
             const int n0 = ti.nt * 128 + 64 * half;
-            // the staged bias is visible once all epilogue warps passed the previous
-            // tile's amax barrier (gate/up) or this tile's first buffer hand-over
-            // ordering; a bounded barrier among the epilogue warps makes it explicit
-            mbar_arrive(smem_u32(&bias_bar));
-            if (!mbar_wait(smem_u32(&bias_bar), tpar, abort_p, err, kErrTimeoutEpilogue)) break;
+            const int bslot = tpar;  // tiles alternate between the two bias slots
+            const uint32_t buse = (uint32_t)(tcount >> 1) & 1u;
+            if (!mbar_wait(smem_u32(&bfull_bar[bslot]), buse, abort_p, err, kErrTimeoutEpilogue)) break;
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
-                acc[i] = s_bias[tpar][64 * half + i];
-                if (GATED) acc[64 + i] = s_bias[tpar][128 + 64 * half + i];
+                acc[i] = s_bias[bslot][64 * half + i];
+                if (GATED) acc[64 + i] = s_bias[bslot][128 + 64 * half + i];
             }
+            mbar_arrive(smem_u32(&bempty_bar[bslot]));
             const float* sa_row = p.sa + grow_c;  // element kb at sa_row[kb * R]
             const float* sw_g = p.sw + ((size_t)ti.e * p.sw_rowblocks + ti.nt) * p.KB;
             // Warps whose TMEM lane quarter holds no valid row of this tile only
@@ -360,20 +379,12 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             if (!ok) break;
             if (tile + (int)gridDim.x < total) {
                 nxt = decode_tile(tile + gridDim.x, s_tiles, s_off, s_cnt, E);
-                stage_bias(nxt, tpar ^ 1u);
                 pre = load_scales(nxt);
             }
 
             if (GATED) {
                 // h = silu(g) * u for this thread's 64 columns of the 128-wide group
-                float amax = 0.f;
-#pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    const float g = acc[i], u = acc[64 + i];
-                    const float h = (n0 + i < p.N_real) ? __fdividef(g, 1.0f + __expf(-g)) * u : 0.f;
-                    acc[i] = h;
-                    amax = fmaxf(amax, fabsf(h));
-                }
+                float amax = swiglu_inplace<64>(acc, acc + 64, p.N_real - n0);
                 // the row's other 64 columns belong to the partner warp (same TMEM
                 // lane quarter); exchange the partial maxima through shared memory,
                 // double-buffered by tile parity, behind a bounded barrier
@@ -384,6 +395,9 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 const float s = group_scale(amax);
                 const float rs = recip_rn(s);
                 if (valid) {
+                    // all 64 quotients first (independent), then the conversions and stores
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) acc[i] = div_by(acc[i], s, rs);
                     uint4* dst = reinterpret_cast<uint4*>(p.hq + (size_t)grow * p.ldq + ti.nt * 128 + 64 * half);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
@@ -391,7 +405,7 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const int i = 16 * v + 4 * q;
-                            w[q] = quant4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3], s, rs);
+                            w[q] = e4m3x2(acc[i], acc[i + 1]) | (e4m3x2(acc[i + 2], acc[i + 3]) << 16);
                         }
                         dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
@@ -399,9 +413,8 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 }
             } else {
                 if (valid) {
-                    const int slot = __ldg(p.perm + grow);
-                    const float w = bf16_bits_to_f32(__ldg(p.topk_wb + slot));
-                    float4* dst = reinterpret_cast<float4*>(p.part + (size_t)slot * p.ldp + n0);
+                    const float w = my_w;
+                    float4* dst = reinterpret_cast<float4*>(p.part + (size_t)my_slot * p.ldp + n0);
 #pragma unroll
                     for (int v = 0; v < 16; ++v)
                         dst[v] = make_float4(w * acc[4 * v], w * acc[4 * v + 1], w * acc[4 * v + 2], w * acc[4 * v + 3]);

@@ -329,14 +329,10 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
             if (GATED) {
                 mbar_arrive(smem_u32(&mempty_bar[slot]));  // this tile's metadata is no longer read
                 // h = silu(g) * u; per-token amax over the 128 features (4 warps x 32 lanes)
+                swiglu_inplace<32>(acc, acc + 32, nvalid ? 32 : 0);
                 float habs[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float g = acc[j], u = acc[32 + j];
-                    const float h = nvalid ? __fdividef(g, 1.0f + __expf(-g)) * u : 0.f;
-                    acc[j] = h;
-                    habs[j] = fabsf(h);
-                }
+                for (int j = 0; j < 32; ++j) habs[j] = fabsf(acc[j]);
                 s_amax[tpar][quarter][lane] = column_max32(habs, lane);  // lane j: this warp's max for token j
                 mbar_arrive(smem_u32(&amax_bar));
                 if (!mbar_wait(smem_u32(&amax_bar), tpar, abort_p, err, kErrTimeoutEpilogue)) break;
@@ -346,12 +342,11 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                 const float r_tok = recip_rn(s_tok);
                 if (quarter == 0 && lane < ti.rows) p.sh[(size_t)ti.nt * p.R + ti.row0 + lane] = s_tok;
 #pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    acc[j] = div_by(acc[j], __shfl_sync(0xffffffffu, s_tok, j), __shfl_sync(0xffffffffu, r_tok, j));
+#pragma unroll
                 for (int j = 0; j < 32; j += 2) {
-                    const float s0 = __shfl_sync(0xffffffffu, s_tok, j);
-                    const float s1 = __shfl_sync(0xffffffffu, s_tok, j + 1);
-                    const float r0 = __shfl_sync(0xffffffffu, r_tok, j);
-                    const float r1 = __shfl_sync(0xffffffffu, r_tok, j + 1);
-                    const uint32_t codes = e4m3x2(div_by(acc[j], s0, r0), div_by(acc[j + 1], s1, r1));
+                    const uint32_t codes = e4m3x2(acc[j], acc[j + 1]);
                     if (j < ti.rows) p.hq[(size_t)(ti.row0 + j) * p.ldq + n] = (uint8_t)(codes & 0xffu);
                     if (j + 1 < ti.rows) p.hq[(size_t)(ti.row0 + j + 1) * p.ldq + n] = (uint8_t)(codes >> 8);
                 }

@@ -38,6 +38,14 @@ struct PermuteParams {
     int tokens_per_cta;
     const int32_t* topk_idx;
     const int32_t* chunk_base;
+    // decode-sized batches: the router did not scan the histogram, this kernel does
+    int scan_here, nchunks, bm, nt1, nt2;
+    const int32_t* hist;
+    int32_t* count;
+    int32_t* offset;
+    int32_t* tiles1;
+    int32_t* tiles2;
+    uint32_t* status;
     int32_t* perm;
     int32_t* inv;
     int R;        // T * k
@@ -85,6 +93,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+bool router_uses_mma(int T, int H);
 cudaError_t launch_router(const RouteParams& p, cudaStream_t st);
 cudaError_t launch_permute_quant(const PermuteParams& p, cudaStream_t st);
 cudaError_t launch_combine(const float* part, int T, int H, int ldp, int k, uint16_t* out, int num_sms,

@@ -19,11 +19,12 @@ namespace moe {
 // selected experts"), rounded to bf16 for the combine ("expert weights in
 // bfloat16").  Two kernels compute the logits:
 //   decode-sized T: router_gemv_kernel, one warp per (token, expert), every
-//     load of a warp in flight at once; the last CTA of a token selects;
+//     load of a warp in flight at once; the last CTA of a token selects, and
+//     the permutation kernel scans the (few-chunk) histogram itself;
 //   prefill-sized T: router_mma_kernel, bf16 mma.sync tiles of 32 tokens x
-//     all experts, selection in the same CTA.
-// In both, the last CTA to finish turns the (chunk, expert) histogram into
-// the per-expert row offsets, per-chunk row bases and GEMM tile lists.
+//     all experts, selection in the same CTA; the last CTA to finish turns
+//     the (chunk, expert) histogram into the per-expert row offsets,
+//     per-chunk row bases and GEMM tile lists.
 
 // The k largest of lg[0..E) for one warp (ties -> lower index), ascending.
 __device__ __forceinline__ void select_topk(const float* lg, int E, int k, int lane, int* chosen) {
@@ -161,27 +162,40 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(RouteParams p) {
     if (e < p.E) {
         const uint16_t* wr = p.rw + (size_t)e * p.H;
         float acc = 0.f;
-#pragma unroll 8
-        for (int h = lane * 8; h < Hx; h += 256) {
-            float w[8];
-            if (vec) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(wr + h));
-                const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        if (vec && Hx <= 16 * 256) {
+            // all of this lane's router-weight loads (at most 16 x 16 bytes) are issued at once
+            uint4 wv[16];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    w[2 * i] = __uint_as_float(u[i] << 16);
-                    w[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+            for (int i = 0; i < 16; ++i) {
+                const int h = lane * 8 + i * 256;
+                wv[i] = h < Hx ? __ldg(reinterpret_cast<const uint4*>(wr + h)) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int h = lane * 8 + i * 256;
+                if (h < Hx) {
+                    const uint4 xv = *reinterpret_cast<const uint4*>(xs + h);
+                    const uint32_t xu[4] = {xv.x, xv.y, xv.z, xv.w};
+                    const uint32_t wu[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc = fmaf(__uint_as_float(xu[q] << 16), __uint_as_float(wu[q] << 16), acc);
+                        acc = fmaf(__uint_as_float(xu[q] & 0xffff0000u), __uint_as_float(wu[q] & 0xffff0000u), acc);
+                    }
                 }
-            } else {
+            }
+        } else {
+            for (int h = lane * 8; h < Hx; h += 256) {
+                float w[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) w[i] = (h + i < p.H) ? bf16_bits_to_f32(wr[h + i]) : 0.f;
-            }
-            const uint4 xv = *reinterpret_cast<const uint4*>(xs + h);
-            const uint32_t u[4] = {xv.x, xv.y, xv.z, xv.w};
+                const uint4 xv = *reinterpret_cast<const uint4*>(xs + h);
+                const uint32_t u[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc = fmaf(__uint_as_float(u[i] << 16), w[2 * i], acc);
-                acc = fmaf(__uint_as_float(u[i] & 0xffff0000u), w[2 * i + 1], acc);
+                for (int i = 0; i < 4; ++i) {
+                    acc = fmaf(__uint_as_float(u[i] << 16), w[2 * i], acc);
+                    acc = fmaf(__uint_as_float(u[i] & 0xffff0000u), w[2 * i + 1], acc);
+                }
             }
         }
 #pragma unroll
@@ -198,7 +212,7 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(RouteParams p) {
         select_topk(s_lg, p.E, p.k, lane, chosen);
         write_route(p, t, s_lg, chosen, lane);
     }
-    if (last_to_arrive(p.done, p.T)) finish_scan(p);
+    // the permutation kernel turns the histogram into offsets (few chunks at these sizes)
 }
 
 // ---- prefill-sized batches: 32 tokens x all experts per CTA on bf16 mma.sync ----
@@ -354,8 +368,10 @@ cudaError_t launch_router(const RouteParams& p, cudaStream_t st) {
 // (token, 128-group) item is quantised by one warp: amax, s = amax/448,
 // code = e4m3(x/s), written to each of the token's k rows.
 __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
-    pdl_wait();
+    extern __shared__ __align__(16) uint8_t psm[];
+    uint16_t* xs = reinterpret_cast<uint16_t*>(psm);  // this CTA's x rows, [tokens_per_cta][Hx]
     __shared__ int s_pre[kMaxExperts];
+    __shared__ int s_base[kMaxExperts];
     __shared__ int s_idx[8 * kMaxTopK];
     __shared__ int s_row[8 * kMaxTopK];
     const int tpc = p.tokens_per_cta;
@@ -363,14 +379,94 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
     const int chunk = t0 / kChunkTokens;
     const int c0 = chunk * kChunkTokens;
     const int nt = min(tpc, p.T - t0);
+    const int Hx = (p.H + 7) & ~7;
+    // x is an input of the layer, not an output of the router: stage it
+    // before waiting for the router to finish
+    if ((p.H & 7) == 0) {
+        for (int i = threadIdx.x; i < nt * Hx / 8; i += blockDim.x)
+            reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t0 * p.H) + i);
+    } else {
+        for (int i = threadIdx.x; i < nt * Hx; i += blockDim.x) {
+            const int tt = i / Hx, h = i - tt * Hx;
+            xs[i] = h < p.H ? p.x[(size_t)(t0 + tt) * p.H + h] : (uint16_t)0;
+        }
+    }
+    pdl_wait();
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) s_pre[e] = 0;
+    if (p.scan_here) {
+        // offsets from the (chunk, expert) histogram: count[e], its exclusive
+        // scan, and the first row of this chunk for every expert
+        for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+            int before = 0, total = 0;
+            for (int c = 0; c < p.nchunks; ++c) {
+                const int h = __ldcg(&p.hist[(size_t)c * p.E + e]);
+                if (c < chunk) before += h;
+                total += h;
+            }
+            s_base[e] = before;
+            s_pre[e] = total;  // reused below as the prefix counter; counts kept in s_base/offset
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            // exclusive scans over the experts by one warp: lane l owns experts [8l, 8l+8)
+            const int lane = threadIdx.x;
+            int cnt[8], mt[8];
+            int tc = 0, tm = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane * 8 + i;
+                cnt[i] = e < p.E ? s_pre[e] : 0;
+                mt[i] = (cnt[i] + p.bm - 1) / p.bm;
+                tc += cnt[i];
+                tm += mt[i];
+            }
+            int ic = tc, im = tm;  // inclusive scans of the lane totals
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int vc = __shfl_up_sync(0xffffffffu, ic, o);
+                const int vm = __shfl_up_sync(0xffffffffu, im, o);
+                if (lane >= o) {
+                    ic += vc;
+                    im += vm;
+                }
+            }
+            int off = ic - tc, mts = im - tm;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane * 8 + i;
+                if (e < p.E) {
+                    s_base[e] += off;
+                    if (blockIdx.x == 0) {
+                        p.offset[e] = off;
+                        p.count[e] = cnt[i];
+                        p.tiles1[e] = mts * p.nt1;
+                        p.tiles2[e] = mts * p.nt2;
+                    }
+                }
+                off += cnt[i];
+                mts += mt[i];
+            }
+            if (blockIdx.x == 0 && lane == 31) {
+                p.offset[p.E] = off;
+                p.tiles1[p.E] = mts * p.nt1;
+                p.tiles2[p.E] = mts * p.nt2;
+                p.status[kStatusTiles1] = (uint32_t)(mts * p.nt1);
+                p.status[kStatusTiles2] = (uint32_t)(mts * p.nt2);
+                p.status[kStatusTileRows] = (uint32_t)p.bm;
+            }
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < p.E; e += blockDim.x) s_pre[e] = 0;
+    } else {
+        for (int e = threadIdx.x; e < p.E; e += blockDim.x) s_base[e] = p.chunk_base[(size_t)chunk * p.E + e];
+    }
     __syncthreads();
     for (int i = threadIdx.x; i < (t0 - c0) * p.k; i += blockDim.x) atomicAdd(&s_pre[p.topk_idx[(size_t)c0 * p.k + i]], 1);
     for (int i = threadIdx.x; i < nt * p.k; i += blockDim.x) s_idx[i] = p.topk_idx[(size_t)t0 * p.k + i];
     __syncthreads();
     for (int i = threadIdx.x; i < nt * p.k; i += blockDim.x) {
         int tt = i / p.k, j = i - tt * p.k, e = s_idx[i];
-        int r = p.chunk_base[(size_t)chunk * p.E + e] + s_pre[e];
+        int r = s_base[e] + s_pre[e];
         for (int u = 0; u < tt; ++u)
             for (int jj = 0; jj < p.k; ++jj) r += (s_idx[u * p.k + jj] == e);
         s_row[i] = r;
@@ -382,22 +478,19 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
 
     const int G = p.Hp / 128;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool vec = (p.H & 3) == 0;
     for (int item = warp; item < nt * G; item += 8) {
         const int tt = item / G, g = item - tt * G;
-        const int t = t0 + tt;
         const int c = g * 128 + lane * 4;
-        float a[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint16_t* xr = p.x + (size_t)t * p.H;
-        if (vec && c + 4 <= p.H) {
-            uint2 v = __ldg(reinterpret_cast<const uint2*>(xr + c));
+        float a[4];
+        if (c + 4 <= Hx) {
+            const uint2 v = *reinterpret_cast<const uint2*>(xs + tt * Hx + c);
             a[0] = __uint_as_float(v.x << 16);
             a[1] = __uint_as_float(v.x & 0xffff0000u);
             a[2] = __uint_as_float(v.y << 16);
             a[3] = __uint_as_float(v.y & 0xffff0000u);
         } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = (c + i < p.H) ? bf16_bits_to_f32(xr[c + i]) : 0.f;
+            for (int i = 0; i < 4; ++i) a[i] = (c + i < Hx) ? bf16_bits_to_f32(xs[tt * Hx + c + i]) : 0.f;
         }
         float amax = fmaxf(fmaxf(fabsf(a[0]), fabsf(a[1])), fmaxf(fabsf(a[2]), fabsf(a[3])));
 #pragma unroll
@@ -414,7 +507,10 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
 
 cudaError_t launch_permute_quant(const PermuteParams& p, cudaStream_t st) {
     int grid = (p.T + p.tokens_per_cta - 1) / p.tokens_per_cta;
-    return launch_pdl(permute_quant_kernel, dim3(grid), dim3(256), 0, st, p);
+    const size_t sm = (size_t)p.tokens_per_cta * ((p.H + 7) & ~7) * 2;
+    cudaError_t e = cudaFuncSetAttribute(permute_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(permute_quant_kernel, dim3(grid), dim3(256), sm, st, p);
 }
 
 // ================================================================= combine
