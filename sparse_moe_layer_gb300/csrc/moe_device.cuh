@@ -37,41 +37,68 @@ __device__ __forceinline__ float group_scale(float amax) { return amax == 0.0f ?
 // rem = v - q0*s (exact with one FMA), q = RN(q0 + rem*r) -- Markstein's
 // correction step (P. Markstein, "Computation of elementary functions on the
 // IBM RISC System/6000 processor", IBM J. Res. Dev. 1990).  The remainder is
-// exact only while it stays in the normal range, so the step is taken for
-// |v| >= 2^-96 (then s >= |v|/448 is normal as well); zeros (whose sign the
-// step would lose), tiny values and NaN take IEEE division.  Checked
-// bit-for-bit against IEEE division by the quantiser tests.
+// exact while it stays in the normal range, which holds for |v| >= 2^-96
+// (then s >= |v|/448 is normal as well).  The quantisers divide every value
+// of a 1x128 group by the group's scale s = amax/448, and when amax >= 2^-64
+// the values below 2^-96 have |v/s| < 448*2^-32, far below half the smallest
+// e4m3 subnormal (2^-10): their code is the signed zero whatever the step
+// returns, as long as the sign is v's.  So div_fast ends by setting the sign
+// bit from v (keep = sign_keep(amax)), which also keeps the sign of -0; in an
+// all-zero group (amax = 0, s = 1) it clears the sign instead, so that every
+// code of that group is +0.  Groups with 0 < amax < 2^-64 take IEEE division
+// (quot_fast false).  Either way the e4m3 codes are those of the correctly
+// rounded quotient, bit for bit (checked by the quantiser tests, tiny,
+// all-zero and signed-zero groups included).
 __device__ __forceinline__ float recip_rn(float s) { return __frcp_rn(s); }
-__device__ __forceinline__ float div_by(float v, float s, float r) {
-    if (!(fabsf(v) >= 0x1p-96f)) return __fdiv_rn(v, s);
+__device__ __forceinline__ bool quot_fast(float amax) { return !(amax > 0.0f && amax < 0x1p-64f); }
+__device__ __forceinline__ uint32_t sign_keep(float amax) { return amax == 0.0f ? 0u : 0x80000000u; }
+__device__ __forceinline__ float div_fast(float v, float s, float r, uint32_t keep) {
     const float q0 = __fmul_rn(v, r);
     const float rem = __fmaf_rn(-q0, s, v);
-    return __fmaf_rn(rem, r, q0);
+    const float q = __fmaf_rn(rem, r, q0);
+    return __uint_as_float((__float_as_uint(q) & 0x7fffffffu) | (__float_as_uint(v) & keep));
 }
 
-// Four values of one group -> four e4m3 codes (byte i = value i): e4m3(v/s),
-// v/s correctly rounded in fp32 (r = recip_rn(s)).
-__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float s, float r) {
-    uint32_t lo = e4m3x2(div_by(a, s, r), div_by(b, s, r));
-    uint32_t hi = e4m3x2(div_by(c, s, r), div_by(d, s, r));
-    return lo | (hi << 16);
+// Four values of a group with absolute maximum amax, scale s = group_scale(amax)
+// and r = recip_rn(s) -> four e4m3 codes (byte i = value i).
+__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float amax, float s, float r) {
+    if (quot_fast(amax)) {
+        const uint32_t k = sign_keep(amax);
+        return e4m3x2(div_fast(a, s, r, k), div_fast(b, s, r, k)) |
+               (e4m3x2(div_fast(c, s, r, k), div_fast(d, s, r, k)) << 16);
+    }
+    return e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s)) | (e4m3x2(__fdiv_rn(c, s), __fdiv_rn(d, s)) << 16);
 }
 
-// h[i] = silu(g[i]) * u[i] = g/(1+exp(-g)) * u for i < N, written over g;
-// h = 0 for i >= n_valid (padding features).  Returns max_i |h[i]|.  The work
-// is issued in independent batches of 16 with four partial maxima, so the two
-// special-function operations per element overlap instead of forming one
-// long dependent chain.
+// 2^x and 1/x from the special-function unit (PTX ex2.approx / rcp.approx,
+// subnormals flushed): one instruction each, no branches.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// h[i] = silu(g[i]) * u[i] = g * u / (1 + e^-g) for i < N, written over g;
+// h = 0 for i >= n_valid (padding features).  Returns max_i |h[i]|.
+// e^-g = 2^(-g log2 e); both special-function operations are the hardware
+// approximations (a few ulp, no branches), issued in independent batches of
+// 16 so they overlap.
 template <int N>
 __device__ __forceinline__ float swiglu_inplace(float* g, const float* u, int n_valid) {
+    constexpr float kNegLog2e = -1.4426950408889634f;
     float m[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int b = 0; b < N; b += 16) {
         float e[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) e[i] = __expf(-g[b + i]);
+        for (int i = 0; i < 16; ++i) e[i] = ex2_approx(g[b + i] * kNegLog2e);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) e[i] = __frcp_rn(1.0f + e[i]);
+        for (int i = 0; i < 16; ++i) e[i] = rcp_approx(1.0f + e[i]);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const float h = (b + i < n_valid) ? g[b + i] * e[i] * u[b + i] : 0.f;
@@ -165,6 +192,14 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
 
 // 2D tiled load of one box (inner coordinate x in elements, row y) into
 // shared memory, completing transaction bytes on mbarrier `bar`.
+// Brings one box of a tiled tensor into L2 without shared memory or a barrier
+// (no completion to wait for); out-of-range parts of the box are skipped.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y, uint32_t bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"

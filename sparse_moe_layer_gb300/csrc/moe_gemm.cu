@@ -45,20 +45,22 @@ struct GemmCfg {
     static constexpr int NBUF = 512 / BN;  // TMEM partial buffers (all 512 columns)
     static constexpr int EPI_WARPS = 8;                   // warpgroups 1 and 2
     static constexpr int THREADS = (4 + EPI_WARPS) * 32;  // warpgroup 0: producer, MMA, 2 idle warps
-    // gate/up: the promotion warps hold 128 accumulators + 64 loaded columns, so
-    // warpgroup 0 hands registers to them: 4*32*(168-56) = 8*32*(224-168)
+    // gate/up: the promotion warps hold 128 accumulators + 32 loaded columns, so
+    // warpgroup 0 hands registers to them; the split must not ask for more than
+    // it frees: 8*32*(208-168) = 10240 <= 4*32*(168-72) = 12288
     static constexpr int LAUNCH_REGS = 168;
-    static constexpr int WG0_REGS = 56;
-    static constexpr int EPI_REGS = 224;
+    static constexpr int WG0_REGS = 72;
+    static constexpr int EPI_REGS = 208;
     static constexpr int COLS = BN / 2;  // accumulator columns per epilogue thread
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
-    static constexpr uint32_t IDESC = idesc_e4m3_f32(BM, 128);  // one MMA half: 128 columns
-    static constexpr int HALVES = BN / 128;                      // gate/up: 2 halves with their own barriers
+    static constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
+    static constexpr int HALVES = BN / 128;  // 128-column blocks of a tile (gate/up: gate and up)
 };
 
 struct TileInfo {
     int e, nt, row0, rows;
 };
+
 
 __device__ __forceinline__ TileInfo decode_tile(int tile, const int* s_tiles, const int* s_off, const int* s_cnt,
                                                 int E) {
@@ -91,8 +93,8 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
 
     __shared__ __align__(8) uint64_t full_bar[C::STAGES];
     __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
-    __shared__ __align__(8) uint64_t tfull_bar[C::NBUF][C::HALVES];
-    __shared__ __align__(8) uint64_t tempty_bar[C::NBUF][C::HALVES];
+    __shared__ __align__(8) uint64_t tfull_bar[C::NBUF];
+    __shared__ __align__(8) uint64_t tempty_bar[C::NBUF];
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ __align__(8) uint64_t amax_bar;  // gate/up epilogue: the two column halves of a row meet here
     __shared__ __align__(8) uint64_t bfull_bar[2];   // bias slot filled by the metadata warp
@@ -110,11 +112,10 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
         }
-        for (int b = 0; b < C::NBUF; ++b)
-            for (int h = 0; h < C::HALVES; ++h) {
-                mbar_init(smem_u32(&tfull_bar[b][h]), 1);
-                mbar_init(smem_u32(&tempty_bar[b][h]), C::EPI_WARPS);
-            }
+        for (int b = 0; b < C::NBUF; ++b) {
+            mbar_init(smem_u32(&tfull_bar[b]), 1);
+            mbar_init(smem_u32(&tempty_bar[b]), C::EPI_WARPS);
+        }
         mbar_init(smem_u32(&drain_bar), 1);
         mbar_init(smem_u32(&amax_bar), C::EPI_WARPS * 32);
         for (int b = 0; b < 2; ++b) {
@@ -159,11 +160,11 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             uint32_t phase = 0;
             uint32_t filled = 0;  // bit s: stage s was filled at least once
             bool ok = true;
+            const int ublk = GATED ? (p.up_rows / 128) * p.KB : 0;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const TileInfo ti = decode_tile(tile, s_tiles, s_off, s_cnt, E);
                 // blocked weights: block (e, row block, kb) starts at row ((e*RB + rb)*KB + kb)*128
                 const int bblk = (ti.e * p.sw_rowblocks + ti.nt) * p.KB;
-                const int ublk = GATED ? (p.up_rows / 128) * p.KB : 0;
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) {
                         ok = false;
@@ -217,23 +218,19 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                     }
                     const uint32_t a_base = smem_u32(smem + stage * C::STAGE_BYTES);
                     const uint32_t b_base = a_base + C::A_BYTES;
-                    // gate/up: the gate half and the up half of the accumulator are
-                    // handed to the promotion warps separately, so one half is
-                    // promoted while the tensor core works on the other
-#pragma unroll
-                    for (int h = 0; h < C::HALVES; ++h) {
-                        if (!mbar_wait(smem_u32(&tempty_bar[buf][h]), tphase ^ 1u, abort_p, err, kErrTimeoutMma)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t d = tmem_base + (uint32_t)(buf * C::BN + 128 * h);
-#pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4)
-                            mma_e4m3(d, smem_desc_sw128(a_base + 32 * k4), smem_desc_sw128(b_base + 128 * 128 * h + 32 * k4),
-                                     C::IDESC, k4 > 0 ? 1u : 0u);
-                        mma_commit(smem_u32(&tfull_bar[buf][h]));
+                    // one N = BN MMA per K step (gate/up: the 128 gate and the 128 up
+                    // weight rows are one 256-row B operand)
+                    if (!mbar_wait(smem_u32(&tempty_bar[buf]), tphase ^ 1u, abort_p, err, kErrTimeoutMma)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + (uint32_t)(buf * C::BN);
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4)
+                        mma_e4m3(d, smem_desc_sw128(a_base + 32 * k4), smem_desc_sw128(b_base + 32 * k4), C::IDESC,
+                                 k4 > 0 ? 1u : 0u);
+                    mma_commit(smem_u32(&tfull_bar[buf]));
                     if (!ok) break;
                     mma_commit(smem_u32(&empty_bar[stage]));
                     if (++stage == C::STAGES) {
@@ -346,28 +343,29 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                     g2 = __ldg(sw_g + kb + 2);
                     if (GATED) u2 = __ldg(sw_g + up_off + kb + 2);
                 }
+                if (!mbar_wait(smem_u32(&tfull_bar[buf]), tphase, abort_p, err, kErrTimeoutEpilogue)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (active) {
 #pragma unroll
-                for (int h = 0; h < C::HALVES; ++h) {
-                    if (!mbar_wait(smem_u32(&tfull_bar[buf][h]), tphase, abort_p, err, kErrTimeoutEpilogue)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (active) {
-                        uint32_t r[64];
-                        tmem_ld64(t_lane + (uint32_t)(buf * C::BN + 128 * h + 64 * half), r);
+                    for (int c = 0; c < 2 * C::HALVES; ++c) {  // 32-column pieces of each 128-column block
+                        const int h = c >> 1;
+                        uint32_t r[32];
+                        tmem_ld32(t_lane + (uint32_t)(buf * C::BN + 128 * h + 64 * half + 32 * (c & 1)), r);
                         const float f = a0 * (h == 0 ? g0 : u0);
                         const float2 f2 = make_float2(f, f);
-                        float2* a2p = reinterpret_cast<float2*>(acc + 64 * h);
+                        float2* a2p = reinterpret_cast<float2*>(acc + 32 * c);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
+                        for (int i = 0; i < 16; ++i)
                             a2p[i] = __ffma2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), f2,
                                                 a2p[i]);
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[buf][h]));
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[buf]));
                 if (!ok) break;
                 if (++buf == C::NBUF) {
                     buf = 0;
@@ -396,8 +394,14 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 const float rs = recip_rn(s);
                 if (valid) {
                     // all 64 quotients first (independent), then the conversions and stores
+                    if (quot_fast(amax)) {
+                        const uint32_t keep = sign_keep(amax);
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) acc[i] = div_by(acc[i], s, rs);
+                        for (int i = 0; i < 64; ++i) acc[i] = div_fast(acc[i], s, rs, keep);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) acc[i] = __fdiv_rn(acc[i], s);
+                    }
                     uint4* dst = reinterpret_cast<uint4*>(p.hq + (size_t)grow * p.ldq + ti.nt * 128 + 64 * half);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {

@@ -341,9 +341,16 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                 const float s_tok = group_scale(amax);  // lane j: scale of token j
                 const float r_tok = recip_rn(s_tok);
                 if (quarter == 0 && lane < ti.rows) p.sh[(size_t)ti.nt * p.R + ti.row0 + lane] = s_tok;
+                if (__all_sync(0xffffffffu, quot_fast(amax))) {
+                    const uint32_t k_tok = sign_keep(amax);
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    acc[j] = div_by(acc[j], __shfl_sync(0xffffffffu, s_tok, j), __shfl_sync(0xffffffffu, r_tok, j));
+                    for (int j = 0; j < 32; ++j)
+                        acc[j] = div_fast(acc[j], __shfl_sync(0xffffffffu, s_tok, j), __shfl_sync(0xffffffffu, r_tok, j),
+                                          __shfl_sync(0xffffffffu, k_tok, j));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[j] = __fdiv_rn(acc[j], __shfl_sync(0xffffffffu, s_tok, j));
+                }
 #pragma unroll
                 for (int j = 0; j < 32; j += 2) {
                     const uint32_t codes = e4m3x2(acc[j], acc[j + 1]);

@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         const float s = group_scale(amax);
-        const uint32_t q = quant4(a[0], a[1], a[2], a[3], s, recip_rn(s));
+        const uint32_t q = quant4(a[0], a[1], a[2], a[3], amax, s, recip_rn(s));
         for (int j = 0; j < p.k; ++j) {
             const int r = s_row[tt * p.k + j];
             *reinterpret_cast<uint32_t*>(p.xq + (size_t)r * p.Hp + c) = q;
@@ -604,7 +604,7 @@ __global__ void __launch_bounds__(256) pack_blocks_kernel(const float* __restric
     const float rc = recip_rn(sc);
     uint32_t packed[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) packed[i] = quant4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], sc, rc);
+    for (int i = 0; i < 16; ++i) packed[i] = quant4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], amax, sc, rc);
     // blocked layout: block (e, bi, bj) is 16 KB contiguous, row-major inside
     const size_t blk = ((size_t)e * (rows_p / 128) + bi) * (cols_p / 128) + bj;
     uint4* dst = reinterpret_cast<uint4*>(q + blk * 16384 + (size_t)r_local * 128 + (threadIdx.x & 1) * 64);
@@ -637,7 +637,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const float* __restr
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         const float sc = group_scale(amax);
-        *reinterpret_cast<uint32_t*>(q + (size_t)r * cp + c) = quant4(a[0], a[1], a[2], a[3], sc, recip_rn(sc));
+        *reinterpret_cast<uint32_t*>(q + (size_t)r * cp + c) = quant4(a[0], a[1], a[2], a[3], amax, sc, recip_rn(sc));
         if (lane == 0) s[(size_t)r * G + g] = sc;
     }
 }

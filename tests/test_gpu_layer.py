@@ -94,6 +94,14 @@ def test_quantize_rows_bit_exact(moe):
     v[6, :7] = np.float32([448.0, -448.0, 1e-30, -1e-30, 2.0 ** -9, 3.0, -0.0])
     v[7, :5] = np.float32([-0.0, 1e-39, -1e-39, 2.0 ** -100, -(2.0 ** -110)])  # signed zero, subnormals, tiny
     v[8, :128] = np.float32(2.0 ** -120) * np.linspace(-1, 1, 128, dtype=np.float32)  # a whole group of tiny values
+    # groups at the edge of the branch-free division's range (amax = 2^-64 and just below), with values
+    # under 2^-96 and signed zeros inside them, and a group of negative zeros only
+    v[9, :128] = np.float32(2.0 ** -64) * np.linspace(-1, 1, 128, dtype=np.float32)
+    v[9, :6] = np.float32([2.0 ** -64, 2.0 ** -97, -(2.0 ** -97), -0.0, 1e-45, -1e-45])
+    v[9, 128:256] = np.float32(np.nextafter(np.float32(2.0 ** -64), np.float32(0))) * np.linspace(-1, 1, 128,
+                                                                                                 dtype=np.float32)
+    v[10, 256:] = -0.0
+    v[11, :4] = np.float32([3e38, -3e38, 1e-40, -2.0 ** -96])
     q, s = moe.quantize_rows(torch.from_numpy(v).cuda())
     qo, so = oracle.quant_rows_f32(v)
     qg = q.cpu().numpy()
