@@ -69,13 +69,12 @@ typedef enum {
 typedef struct {
     size_t total_bytes;
     size_t status;     /* uint32[64]: [0] device error word, [1] tile total GEMM1, [2] tile total GEMM2 */
-    size_t hist;       /* int32 [ceil(T/256), E] tokens per (256-token chunk, expert), then 1 + T arrival counters */
+    size_t hist;       /* int32 [ceil(T/256), E] tokens per (256-token chunk, expert), then 1 arrival counter */
     size_t count;      /* int32 [E]     rows per expert */
     size_t offset;     /* int32 [E+1]   first row of each expert (exclusive scan of count) */
     size_t chunk_base; /* int32 [ceil(T/256), E] first row of each (chunk, expert) */
     size_t tiles1;     /* int32 [E+1]   first gate/up GEMM tile of each expert */
     size_t tiles2;     /* int32 [E+1]   first down GEMM tile of each expert */
-    size_t logits;     /* float [T, E] router logits (decode-sized batches only) */
     size_t topk_idx;   /* int32 [T, top_k] selected experts, ascending */
     size_t topk_w;     /* float [T, top_k] softmax weights before bf16 rounding */
     size_t topk_wb;    /* bf16  [T, top_k] routing weights used by the layer */
@@ -103,8 +102,8 @@ moe_status moe_get_workspace_layout(int T, int H, int I, int E, int top_k, moe_w
  *   b2       bf16 [E, H]
  *   out      bf16 [T, H]
  *   workspace: device buffer of at least moe_workspace_size(...) bytes, 256-byte aligned.
- * All pointers are device pointers; x, w13, w2, out and the workspace must be
- * 16-byte aligned.  stream is a cudaStream_t (NULL = legacy default stream).
+ * All pointers are device pointers; x, router_w, w13, w2, out and the
+ * workspace must be 16-byte aligned.  stream is a cudaStream_t (NULL = legacy default stream).
  */
 moe_status moe_forward(const void* x, const void* router_w, const void* router_b, const uint8_t* w13, const float* s13,
                        const void* b13, const uint8_t* w2, const float* s2, const void* b2, int T, int H, int I, int E,

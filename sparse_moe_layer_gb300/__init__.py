@@ -29,8 +29,7 @@ class MoeError(RuntimeError):
         self.code = code
 
 
-_LAYOUT_FIELDS = ["total_bytes", "status", "hist", "count", "offset", "chunk_base", "tiles1", "tiles2", "logits",
-                  "topk_idx",
+_LAYOUT_FIELDS = ["total_bytes", "status", "hist", "count", "offset", "chunk_base", "tiles1", "tiles2", "topk_idx",
                   "topk_w", "topk_wb", "perm", "inv", "xq", "sx", "hq", "sh", "part"]
 
 
@@ -132,7 +131,6 @@ def workspace_views(ws: torch.Tensor, T: int, H: int, I: int, E: int, top_k: int
         chunk_base=v("chunk_base", nch * E, torch.int32, (nch, E)),
         tiles1=v("tiles1", E + 1, torch.int32, (E + 1,)),
         tiles2=v("tiles2", E + 1, torch.int32, (E + 1,)),
-        logits=v("logits", T * E, torch.float32, (T, E)),
         topk_idx=v("topk_idx", R, torch.int32, (T, top_k)),
         topk_w=v("topk_w", R, torch.float32, (T, top_k)),
         topk_wb=v("topk_wb", R, torch.bfloat16, (T, top_k)),

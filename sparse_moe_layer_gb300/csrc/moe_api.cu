@@ -40,13 +40,12 @@ void layout_of(int T, int H, int I, int E, int k, moe_workspace_layout* L) {
         return at;
     };
     L->status = take(kStatusWords * 4);
-    L->hist = take((nch * E + 1 + (size_t)T) * 4);  // + arrival counter + per-token counters
+    L->hist = take((nch * E + 1) * 4);  // + arrival counter of the router CTAs
     L->count = take((size_t)E * 4);
     L->offset = take((size_t)(E + 1) * 4);
     L->chunk_base = take(nch * E * 4);
     L->tiles1 = take((size_t)(E + 1) * 4);
     L->tiles2 = take((size_t)(E + 1) * 4);
-    L->logits = take((size_t)T * E * 4);
     L->topk_idx = take(R * 4);
     L->topk_w = take(R * 4);
     L->topk_wb = take(R * 2);
@@ -153,7 +152,7 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     if (!x || !router_w || !router_b || !w13 || !s13 || !b13 || !w2 || !s2 || !b2 || !out || !workspace)
         return MOE_ERR_INVALID_ARG;
     if (!sizes_ok(T, H, I, E, top_k)) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(out) ||
+    if (!aligned16(x) || !aligned16(router_w) || !aligned16(w13) || !aligned16(w2) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return MOE_ERR_UNSUPPORTED;
     moe_workspace_layout L;
@@ -190,8 +189,7 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     rp.topk_wb = reinterpret_cast<uint16_t*>(ws + L.topk_wb);
     rp.hist = reinterpret_cast<int32_t*>(ws + L.hist);
     rp.done = rp.hist + (size_t)nch * E;
-    rp.tok_cnt = rp.done + 1;
-    rp.logits = reinterpret_cast<float*>(ws + L.logits);
+    rp.scan_in_router = router_scans(T) ? 1 : 0;
     rp.count = reinterpret_cast<int32_t*>(ws + L.count);
     rp.offset = reinterpret_cast<int32_t*>(ws + L.offset);
     rp.chunk_base = reinterpret_cast<int32_t*>(ws + L.chunk_base);
@@ -212,7 +210,7 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     pp.tokens_per_cta = (T > 2048 && 8LL * ((H + 7) & ~7) * 2 <= 96 * 1024) ? 8 : 1;
     pp.topk_idx = rp.topk_idx;
     pp.chunk_base = rp.chunk_base;
-    pp.scan_here = router_uses_mma(T, H) ? 0 : 1;
+    pp.scan_here = router_scans(T) ? 0 : 1;
     pp.nchunks = nch;
     pp.bm = rp.bm;
     pp.nt1 = rp.nt1;

@@ -21,9 +21,8 @@ struct RouteParams {
     float* topk_w;
     uint16_t* topk_wb;
     int32_t* hist;    // [nchunks, E], zeroed before the launch
-    int32_t* done;    // arrival counter of finished CTAs (or tokens), zeroed before the launch
-    int32_t* tok_cnt; // [T] per-token arrival counters (split-expert path), zeroed before the launch
-    float* logits;    // [T, E] fp32 (split-expert path)
+    int32_t* done;    // arrival counter of finished router CTAs, zeroed before the launch
+    int scan_in_router;  // 1: the last router CTA scans the histogram (else the permutation kernel does)
     int32_t* count;
     int32_t* offset;
     int32_t* chunk_base;
@@ -93,7 +92,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-bool router_uses_mma(int T, int H);
+bool router_scans(int T);  // large batches: the router scans, small ones: the permutation kernel
 cudaError_t launch_router(const RouteParams& p, cudaStream_t st);
 cudaError_t launch_permute_quant(const PermuteParams& p, cudaStream_t st);
 cudaError_t launch_combine(const float* part, int T, int H, int ldp, int k, uint16_t* out, int num_sms,

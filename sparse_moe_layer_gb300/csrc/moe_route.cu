@@ -17,14 +17,11 @@ namespace moe {
 // expert index) are stored in ascending expert order with the softmax over
 // their k logits in fp32 ("softmax after top-k", "softmax only over the
 // selected experts"), rounded to bf16 for the combine ("expert weights in
-// bfloat16").  Two kernels compute the logits:
-//   decode-sized T: router_gemv_kernel, one warp per (token, expert), every
-//     load of a warp in flight at once; the last CTA of a token selects, and
-//     the permutation kernel scans the (few-chunk) histogram itself;
-//   prefill-sized T: router_mma_kernel, bf16 mma.sync tiles of 32 tokens x
-//     all experts, selection in the same CTA; the last CTA to finish turns
-//     the (chunk, expert) histogram into the per-expert row offsets,
-//     per-chunk row bases and GEMM tile lists.
+// bfloat16").  One kernel (router_kernel, below) computes the logits with a
+// thread-block cluster per 32-token tile and selects; for large batches its
+// last CTA also turns the (chunk, expert) histogram into the per-expert row
+// offsets, per-chunk row bases and GEMM tile lists, for small ones the
+// permutation kernel does that itself.
 
 // The k largest of lg[0..E) for one warp (ties -> lower index), ascending.
 __device__ __forceinline__ void select_topk(const float* lg, int E, int k, int lane, int* chosen) {
@@ -142,83 +139,49 @@ __device__ __forceinline__ bool last_to_arrive(int* ctr, int total) {
     return s_last != 0;
 }
 
-// ---- decode-sized batches: grid (T, ceil(E/8)), 8 warps, warp = one expert ----
-__global__ void __launch_bounds__(256) router_gemv_kernel(RouteParams p) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // one x row, zero-padded to Hx
-    const int Hx = (p.H + 7) & ~7;
-    const int t = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool vec = (p.H & 7) == 0;
-    const uint16_t* xr = p.x + (size_t)t * p.H;
-    if (vec) {
-        for (int i = threadIdx.x; i < Hx / 8; i += 256)
-            reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(xr) + i);
-    } else {
-        for (int i = threadIdx.x; i < Hx; i += 256) xs[i] = i < p.H ? xr[i] : (uint16_t)0;
-    }
-    __syncthreads();
-    const int e = blockIdx.y * 8 + warp;
-    if (e < p.E) {
-        const uint16_t* wr = p.rw + (size_t)e * p.H;
-        float acc = 0.f;
-        if (vec && Hx <= 16 * 256) {
-            // all of this lane's router-weight loads (at most 16 x 16 bytes) are issued at once
-            uint4 wv[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int h = lane * 8 + i * 256;
-                wv[i] = h < Hx ? __ldg(reinterpret_cast<const uint4*>(wr + h)) : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int h = lane * 8 + i * 256;
-                if (h < Hx) {
-                    const uint4 xv = *reinterpret_cast<const uint4*>(xs + h);
-                    const uint32_t xu[4] = {xv.x, xv.y, xv.z, xv.w};
-                    const uint32_t wu[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        acc = fmaf(__uint_as_float(xu[q] << 16), __uint_as_float(wu[q] << 16), acc);
-                        acc = fmaf(__uint_as_float(xu[q] & 0xffff0000u), __uint_as_float(wu[q] & 0xffff0000u), acc);
-                    }
-                }
-            }
-        } else {
-            for (int h = lane * 8; h < Hx; h += 256) {
-                float w[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) w[i] = (h + i < p.H) ? bf16_bits_to_f32(wr[h + i]) : 0.f;
-                const uint4 xv = *reinterpret_cast<const uint4*>(xs + h);
-                const uint32_t u[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc = fmaf(__uint_as_float(u[i] << 16), w[2 * i], acc);
-                    acc = fmaf(__uint_as_float(u[i] & 0xffff0000u), w[2 * i + 1], acc);
-                }
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) p.logits[(size_t)t * p.E + e] = acc + bf16_bits_to_f32(p.rb[e]);
-    }
-    if (!last_to_arrive(&p.tok_cnt[t], gridDim.y)) return;
-    // this CTA selects token t
-    __shared__ float s_lg[kMaxExperts];
-    for (int i = threadIdx.x; i < p.E; i += 256) s_lg[i] = __ldcg(&p.logits[(size_t)t * p.E + i]);
-    __syncthreads();
-    if (warp == 0) {
-        int chosen[kMaxTopK];
-        select_topk(s_lg, p.E, p.k, lane, chosen);
-        write_route(p, t, s_lg, chosen, lane);
-    }
-    // the permutation kernel turns the histogram into offsets (few chunks at these sizes)
+// ---- thread-block cluster helpers ----
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+// Every thread of every CTA of the cluster arrives; shared-memory writes made
+// before it are visible to the whole cluster after it.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// A float from the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
 }
 
-// ---- prefill-sized batches: 32 tokens x all experts per CTA on bf16 mma.sync ----
-constexpr int kRtTok = 32;   // tokens per CTA
-constexpr int kRtK = 64;     // K chunk
-constexpr int kRtLd = 72;    // padded smem row (bf16 elements): conflict-free fragment loads
+// ---- router: 32 tokens x all experts per cluster, K split over its CTAs ----
+// A cluster of KS CTAs owns a tile of 32 tokens; CTA r of it accumulates the
+// logits of all experts over its own run of 64-wide K chunks on bf16 mma.sync
+// (fp32 accumulation), with kRtNB chunks of x and router weights in flight.
+// The KS partial tiles are then summed in rank order through distributed
+// shared memory (the same order whatever CTA sums), each CTA finishing the
+// tokens r, r + KS, ...: bias, top-k and softmax for one token per warp.  So
+// small batches spread over up to 8x more SMs than they have token tiles, and
+// no partial logit goes through global memory.
+constexpr int kRtTok = 32;  // tokens per cluster
+constexpr int kRtK = 64;    // K chunk
+constexpr int kRtLd = 72;   // padded smem row (bf16 elements): conflict-free fragment loads
+constexpr int kRtNB = 4;    // chunks in flight per CTA
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
@@ -233,32 +196,52 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int NTW>  // 8-expert n-tiles per warp; experts padded to EP = 64 * NTW
-__global__ void __launch_bounds__(256) router_mma_kernel(RouteParams p) {
-    constexpr int EP = 64 * NTW;
+template <int NTW>
+struct RouterCfg {
+    static constexpr int EP = 64 * NTW;                   // experts padded to 8 warps x NTW n8 tiles
+    static constexpr int CHUNK = (kRtTok + EP) * kRtLd;   // bf16 elements of one staged K chunk
+    static constexpr int LDL = EP + 4;                    // fp32 row of a logit tile
+    static constexpr size_t LOAD_BYTES = (size_t)kRtNB * CHUNK * 2;
+    static constexpr size_t TILE_BYTES = (size_t)2 * kRtTok * LDL * 4;  // partial + finished logits
+    static constexpr size_t SMEM = LOAD_BYTES > TILE_BYTES ? LOAD_BYTES : TILE_BYTES;
+};
+
+// cpc: K chunks per CTA.  VEC: H % 8 == 0 (16-byte cp.async rows).
+template <int NTW, bool VEC>
+__global__ void __launch_bounds__(256) router_kernel(RouteParams p, int cpc) {
+    using C = RouterCfg<NTW>;
+    constexpr int EP = C::EP, LDL = C::LDL;
     extern __shared__ __align__(16) uint8_t smem[];
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                 // [2][kRtTok][kRtLd]
-    uint16_t* ws = xs + 2 * kRtTok * kRtLd;                           // [2][EP][kRtLd]
-    float* lg = reinterpret_cast<float*>(smem);                       // [kRtTok][EP + 4], after the K loop
-    const int t0 = blockIdx.x * kRtTok;
+    uint16_t* cbuf = reinterpret_cast<uint16_t*>(smem);  // [kRtNB][(kRtTok + EP) * kRtLd]
+    const uint32_t rank = cluster_ctarank(), KS = cluster_nctarank();
+    const int t0 = (int)cluster_id_x() * kRtTok;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, c = lane & 3;
     const int nchunk = (p.H + kRtK - 1) / kRtK;
+    const int c0 = (int)rank * cpc;
+    const int nmine = max(0, min(cpc, nchunk - c0));
 
     auto load_chunk = [&](int ch, int buf) {
+        uint16_t* xs = cbuf + buf * C::CHUNK;  // [kRtTok][kRtLd] then [EP][kRtLd]
         const int k0 = ch * kRtK;
-        // x: kRtTok rows x 8 pieces of 16 bytes
-        for (int i = tid; i < kRtTok * 8; i += 256) {
-            const int r = i >> 3, q = i & 7, t = t0 + r, k = k0 + q * 8;
-            const bool ok = t < p.T && k < p.H;
-            cp_async16(smem_u32(xs + (buf * kRtTok + r) * kRtLd + q * 8), ok ? p.x + (size_t)t * p.H + k : p.x, ok);
+        if (VEC) {
+            for (int i = tid; i < (kRtTok + EP) * 8; i += 256) {
+                const int r = i >> 3, q = i & 7, k = k0 + q * 8;
+                const bool isx = r < kRtTok;
+                const int row = isx ? t0 + r : r - kRtTok;
+                const bool ok = (isx ? row < p.T : row < p.E) && k < p.H;
+                const uint16_t* src = isx ? p.x + (size_t)row * p.H + k : p.rw + (size_t)row * p.H + k;
+                cp_async16(smem_u32(xs + r * kRtLd + q * 8), ok ? src : p.x, ok);
+            }
+        } else {
+            for (int i = tid; i < (kRtTok + EP) * kRtK; i += 256) {
+                const int r = i / kRtK, q = i - r * kRtK, k = k0 + q;
+                const bool isx = r < kRtTok;
+                const int row = isx ? t0 + r : r - kRtTok;
+                const bool ok = (isx ? row < p.T : row < p.E) && k < p.H;
+                xs[r * kRtLd + q] = ok ? (isx ? p.x[(size_t)row * p.H + k] : p.rw[(size_t)row * p.H + k]) : (uint16_t)0;
+            }
         }
-        for (int i = tid; i < EP * 8; i += 256) {
-            const int r = i >> 3, q = i & 7, k = k0 + q * 8;
-            const bool ok = r < p.E && k < p.H;
-            cp_async16(smem_u32(ws + (buf * EP + r) * kRtLd + q * 8), ok ? p.rw + (size_t)r * p.H + k : p.rw, ok);
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
     };
 
     float acc[2][NTW][4];
@@ -269,18 +252,18 @@ __global__ void __launch_bounds__(256) router_mma_kernel(RouteParams p) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc[m][j][q] = 0.f;
 
-    load_chunk(0, 0);
-    for (int ch = 0; ch < nchunk; ++ch) {
-        const int buf = ch & 1;
-        if (ch + 1 < nchunk) {
-            load_chunk(ch + 1, buf ^ 1);
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-        } else {
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
-        }
+    // kRtNB chunks in flight; one commit group per chunk slot (empty past the end)
+#pragma unroll
+    for (int i = 0; i < kRtNB; ++i) {
+        if (i < nmine) load_chunk(c0 + i, i);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    for (int i = 0; i < nmine; ++i) {
+        const int buf = i % kRtNB;
+        asm volatile("cp.async.wait_group %0;" ::"n"(kRtNB - 1) : "memory");
         __syncthreads();
-        const uint16_t* xb = xs + buf * kRtTok * kRtLd;
-        const uint16_t* wb = ws + buf * EP * kRtLd;
+        const uint16_t* xb = cbuf + buf * C::CHUNK;
+        const uint16_t* wb = xb + kRtTok * kRtLd;
 #pragma unroll
         for (int ks = 0; ks < kRtK / 16; ++ks) {
             const int kk = ks * 16 + 2 * c;
@@ -304,61 +287,85 @@ __global__ void __launch_bounds__(256) router_mma_kernel(RouteParams p) {
             }
         }
         __syncthreads();
+        if (i + kRtNB < nmine) load_chunk(c0 + i + kRtNB, buf);
+        asm volatile("cp.async.commit_group;" ::: "memory");
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
 
-    // logits (+ bias) into shared memory, then one warp per token selects
-    constexpr int LDL = EP + 4;
+    // this CTA's partial logits (no bias) into shared memory, visible to the cluster
+    float* part = reinterpret_cast<float*>(smem);  // [kRtTok][LDL]
+    float* lg = part + kRtTok * LDL;                // [ceil(kRtTok / KS)][LDL]
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
         for (int j = 0; j < NTW; ++j) {
             const int col = (warp * NTW + j) * 8 + 2 * c;
-            const float b0 = col < p.E ? bf16_bits_to_f32(p.rb[col]) : 0.f;
-            const float b1 = col + 1 < p.E ? bf16_bits_to_f32(p.rb[col + 1]) : 0.f;
             const int row = m * 16 + g;
-            lg[row * LDL + col] = acc[m][j][0] + b0;
-            lg[row * LDL + col + 1] = acc[m][j][1] + b1;
-            lg[(row + 8) * LDL + col] = acc[m][j][2] + b0;
-            lg[(row + 8) * LDL + col + 1] = acc[m][j][3] + b1;
+            part[row * LDL + col] = acc[m][j][0];
+            part[row * LDL + col + 1] = acc[m][j][1];
+            part[(row + 8) * LDL + col] = acc[m][j][2];
+            part[(row + 8) * LDL + col + 1] = acc[m][j][3];
         }
+    cluster_sync_all();
+    // tokens rank, rank + KS, ...: sum the KS partials in rank order, add the bias
+    const int nmy = (kRtTok - (int)rank + (int)KS - 1) / (int)KS;
+    for (int idx = tid; idx < nmy * EP; idx += 256) {
+        const int li = idx / EP, e = idx - li * EP;
+        const int r = (int)rank + li * (int)KS;
+        const uint32_t a = smem_u32(part + r * LDL + e);
+        float sum = 0.f;
+        for (uint32_t q = 0; q < KS; ++q) sum += (q == rank) ? part[r * LDL + e] : ld_cluster_f32(a, q);
+        lg[li * LDL + e] = e < p.E ? sum + bf16_bits_to_f32(p.rb[e]) : -INFINITY;
+    }
     __syncthreads();
-    for (int r = warp; r < kRtTok; r += 8) {
-        const int t = t0 + r;
+    for (int li = warp; li < nmy; li += 8) {
+        const int t = t0 + (int)rank + li * (int)KS;
         if (t >= p.T) break;
         int chosen[kMaxTopK];
-        select_topk(lg + r * LDL, p.E, p.k, lane, chosen);
-        write_route(p, t, lg + r * LDL, chosen, lane);
+        select_topk(lg + li * LDL, p.E, p.k, lane, chosen);
+        write_route(p, t, lg + li * LDL, chosen, lane);
     }
-    if (last_to_arrive(p.done, gridDim.x)) finish_scan(p);
+    // no CTA leaves while another may still read its partial tile
+    cluster_sync_all();
+    if (p.scan_in_router && last_to_arrive(p.done, gridDim.x)) finish_scan(p);
 }
 
-template <int NTW>
-static cudaError_t launch_router_mma(const RouteParams& p, cudaStream_t st) {
-    constexpr int EP = 64 * NTW;
-    size_t loads = (size_t)2 * (kRtTok + EP) * kRtLd * 2;
-    size_t logit = (size_t)kRtTok * (EP + 4) * 4;
-    size_t sm = loads > logit ? loads : logit;
-    cudaError_t e = cudaFuncSetAttribute(router_mma_kernel<NTW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+template <int NTW, bool VEC>
+static cudaError_t launch_router_t(const RouteParams& p, cudaStream_t st) {
+    using C = RouterCfg<NTW>;
+    const int ntiles = (p.T + kRtTok - 1) / kRtTok;
+    const int nchunk = (p.H + kRtK - 1) / kRtK;
+    int ks = ntiles >= 148 ? 1 : 296 / ntiles;  // about two CTAs per SM in all
+    ks = ks < 1 ? 1 : (ks > 8 ? 8 : ks);
+    if (ks > nchunk) ks = nchunk;
+    const int cpc = (nchunk + ks - 1) / ks;
+    ks = (nchunk + cpc - 1) / cpc;  // no CTA without a chunk
+    cudaError_t e = cudaFuncSetAttribute(router_kernel<NTW, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    router_mma_kernel<NTW><<<(p.T + kRtTok - 1) / kRtTok, 256, sm, st>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ntiles * ks);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, router_kernel<NTW, VEC>, p, cpc);
 }
 
-bool router_uses_mma(int T, int H) { return T >= 512 && (H % 8) == 0; }
+bool router_scans(int T) { return T >= 512; }
 
 cudaError_t launch_router(const RouteParams& p, cudaStream_t st) {
-    if (router_uses_mma(p.T, p.H)) {
-        if (p.E <= 64) return launch_router_mma<1>(p, st);
-        if (p.E <= 128) return launch_router_mma<2>(p, st);
-        return launch_router_mma<4>(p, st);
-    }
-    const int Hx = (p.H + 7) & ~7;
-    dim3 grid(p.T, (p.E + 7) / 8);
-    size_t sm = (size_t)Hx * 2;
-    cudaError_t e = cudaFuncSetAttribute(router_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    if (e != cudaSuccess) return e;
-    router_gemv_kernel<<<grid, 256, sm, st>>>(p);
-    return cudaGetLastError();
+    const bool vec = (p.H % 8) == 0;
+    if (p.E <= 64) return vec ? launch_router_t<1, true>(p, st) : launch_router_t<1, false>(p, st);
+    if (p.E <= 128) return vec ? launch_router_t<2, true>(p, st) : launch_router_t<2, false>(p, st);
+    return vec ? launch_router_t<4, true>(p, st) : launch_router_t<4, false>(p, st);
 }
 
 // ======================================================= permute + x quant

@@ -49,7 +49,7 @@ def test_host_argument_checks(moe):
     assert L.moe_workspace_size(64, 256, 256, 300, 2) == 0  # E > 256
     assert L.moe_workspace_size(64, 256, 256, 8, 2) > 0
     lay = moe.workspace_layout(64, 2880, 2880, 32, 4)
-    offs = [lay[k] for k in ("status", "hist", "count", "offset", "chunk_base", "tiles1", "tiles2", "logits", "topk_idx",
+    offs = [lay[k] for k in ("status", "hist", "count", "offset", "chunk_base", "tiles1", "tiles2", "topk_idx",
                              "topk_w", "topk_wb", "perm", "inv", "xq", "sx", "hq", "sh", "part")]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert lay["total_bytes"] >= lay["part"] + 256 * 2944 * 4

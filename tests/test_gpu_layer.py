@@ -169,9 +169,15 @@ def test_equal_logits_pick_lowest_experts(moe):
     assert np.allclose(w, 1.0 / 3.0, rtol=1e-6)
 
 
-def test_many_tokens_uses_blocked_router_and_permute(moe):
-    # T > 2048 switches the router to 4 tokens per CTA and the permutation to 8 tokens per CTA
+def test_many_tokens_router_scan_and_blocked_permute(moe):
+    # T >= 512: the router's last CTA scans the histogram; T > 2048: 8 tokens per permutation CTA;
+    # 79 token tiles: router clusters of 2 CTAs, 2 of the 4 K chunks each
     full_check(moe, _adhoc("many_tokens", 2500, 256, 256, 8, 2), n_sample=48)
+
+
+def test_hidden_size_not_multiple_of_8(moe):
+    # rows of x and of the router weights are not 16-byte aligned: element-wise router loads
+    full_check(moe, _adhoc("odd_hidden", 19, 196, 136, 6, 2))
 
 
 def test_repeated_calls_are_bit_identical(moe):
