@@ -234,8 +234,10 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
 
     CUtensorMap tmA1, tmB1, tmA2, tmB2;
     // weights are blocked: a 2D view of 128-byte rows, one 128x128 block = 128 consecutive rows
-    if (!make_map(&tmA1, pp.xq, R, Hp, rp.bm) || !make_map(&tmB1, w13, (uint64_t)E * 2 * Ip * (Hp / 128), 128) ||
-        !make_map(&tmA2, ws + L.hq, R, Ip, rp.bm) || !make_map(&tmB2, w2, (uint64_t)E * Hp * (Ip / 128), 128))
+    // decode kernels load a tile's activation rows in boxes of kDecXBoxRows, only as many as it has rows
+    const uint32_t a_box = decode ? kDecXBoxRows : (uint32_t)rp.bm;
+    if (!make_map(&tmA1, pp.xq, R, Hp, a_box) || !make_map(&tmB1, w13, (uint64_t)E * 2 * Ip * (Hp / 128), 128) ||
+        !make_map(&tmA2, ws + L.hq, R, Ip, a_box) || !make_map(&tmB2, w2, (uint64_t)E * Hp * (Ip / 128), 128))
         return MOE_ERR_CUDA;
 
     GemmParams g1;

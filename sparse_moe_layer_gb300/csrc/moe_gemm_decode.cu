@@ -8,13 +8,16 @@
 // by streaming the activated experts' weights from HBM ("Hosting Qwen on
 // Blackwell", Decoders: with few tokens the GEMM is limited by loading
 // weights into the tensor cores), so nearly all of every pipeline stage is
-// weight bytes: 5 stages of 32 KB (gate + up) or 10 of 16 KB (down) are in
-// flight per SM, and the small TMEM tiles give 4-8 accumulation buffers, so
-// the scale promotion never stalls the MMA.
+// weight bytes: 5 stages of 32 KB (gate + up) or 9 of 16 KB (down) are in
+// flight per SM -- deeper rings were measured and gain nothing -- and the
+// small TMEM tiles give 8-16 accumulation buffers, so the scale promotion
+// never stalls the MMA.  A tile loads only the 8-row boxes of token rows it
+// has; the metadata slots are sized by the K-block count.
 //
 // Tile = (expert, 128 output features, 32 token rows), ordered expert,
 // n-tile, m-tile; one CTA per SM, persistent.
-//   warp 0     TMA producer (weights: one or two 128x128 boxes; tokens: one 32x128 box)
+//   warp 0     TMA producer (weights: one or two 128x128 boxes; tokens: the
+//              tile's rows in boxes of 8)
 //   warp 1     TMEM allocator and MMA issuer
 //   warps 2-5  promotion + epilogue, one TMEM lane quarter (32 features) each:
 //              gate/up: h = silu(g)*u, 1x128 requant across the 128 features of
@@ -38,29 +41,36 @@ struct DecCfg {
     static constexpr int W_BYTES = (GATED ? 2 : 1) * 128 * 128;
     static constexpr int X_BYTES = BT * 128;
     static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
-    static constexpr int STAGES = GATED ? 5 : 9;
+    static constexpr int MAX_STAGES = 16;                 // the ring takes what shared memory is left (launch)
     static constexpr int ACC_COLS = GATED ? 2 * BT : BT;  // TMEM columns of one accumulation buffer
     static constexpr int TMEM_COLS = 512;
     static constexpr int NBUF = TMEM_COLS / ACC_COLS;     // 8 (gate/up) or 16 (down)
     static constexpr int EPI_WARPS = 4;
     static constexpr int META_WARP = 6;
     static constexpr int THREADS = 7 * 32;
-    static constexpr int KB_MAX = 128;                    // K <= 16384
-    // one metadata slot (floats): bias [256], token scales [KB_MAX][32], weight scales [2][KB_MAX],
-    // token slots [32] (int) and routing weights [32]
-    static constexpr int M_BIAS = 0;
-    static constexpr int M_SA = 256;
-    static constexpr int M_SW = M_SA + KB_MAX * 32;
-    static constexpr int M_SLOT = M_SW + 2 * KB_MAX;
-    static constexpr int M_W = M_SLOT + 32;
-    static constexpr int META_FLOATS = M_W + 32;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 2 * META_FLOATS * 4 + 1024;
     static constexpr uint32_t IDESC = idesc_e4m3_f32(128, BT);
 };
 
 struct DecTile {
     int e, nt, row0, rows;
 };
+
+// One metadata slot (floats), sized by the K-block count: bias [256], token
+// scales [KB][32], weight scales of the gate (or only) block [KB] and of the
+// up block [KB], token slots [32] (int) and routing weights [32].
+struct DecMeta {
+    int sa, sw, swu, slot, w, floats;
+};
+__host__ __device__ inline DecMeta dec_meta(int KB) {
+    DecMeta m;
+    m.sa = 256;
+    m.sw = m.sa + 32 * KB;
+    m.swu = m.sw + KB;
+    m.slot = m.swu + KB;
+    m.w = m.slot + 32;
+    m.floats = (m.w + 32 + 3) & ~3;
+    return m;
+}
 
 __device__ __forceinline__ DecTile decode_dec_tile(int tile, const int* s_tiles, const int* s_off, const int* s_cnt,
                                                    int E) {
@@ -86,14 +96,15 @@ __device__ __forceinline__ DecTile decode_dec_tile(int tile, const int* s_tiles,
 template <bool GATED>
 __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
     moe_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                           const GemmParams p) {
+                           const GemmParams p, const int nst) {
     using C = DecCfg<GATED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    float* meta = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES);  // [2][META_FLOATS]
+    const DecMeta M = dec_meta(p.KB);
+    float* meta = reinterpret_cast<float*>(smem + nst * C::STAGE_BYTES);  // [2][M.floats]
 
-    __shared__ __align__(8) uint64_t full_bar[C::STAGES];
-    __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
+    __shared__ __align__(8) uint64_t full_bar[C::MAX_STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[C::MAX_STAGES];
     __shared__ __align__(8) uint64_t tfull_bar[C::NBUF];
     __shared__ __align__(8) uint64_t tempty_bar[C::NBUF];
     __shared__ __align__(8) uint64_t mfull_bar[2];
@@ -108,7 +119,7 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = p.E;
     if (tid == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < nst; ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
         }
@@ -156,34 +167,39 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                 // blocked weights: block (e, row block, kb) starts at row ((e*RB + rb)*KB + kb)*128
                 const int wblk = (ti.e * p.sw_rowblocks + ti.nt) * p.KB;
                 const int ublk = GATED ? (p.up_rows / 128) * p.KB : 0;
+                const int nxb = (ti.rows + kDecXBoxRows - 1) / kDecXBoxRows;
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = smem_u32(&full_bar[stage]);
-                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    mbar_arrive_expect_tx(fb, C::W_BYTES + nxb * kDecXBoxRows * 128);
                     const uint32_t w_dst = smem_u32(smem + stage * C::STAGE_BYTES);
                     tma_load_2d(w_dst, &tmW, 0, (wblk + kb) * 128, fb);
                     if (GATED) tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb) * 128, fb);
-                    tma_load_2d(w_dst + C::W_BYTES, &tmX, kb * 128, ti.row0, fb);
+                    // only the boxes that hold rows of this tile; the MMA reads stale shared
+                    // memory for the other token columns, whose results are never stored
+                    for (int b = 0; b < nxb; ++b)
+                        tma_load_2d(w_dst + C::W_BYTES + b * kDecXBoxRows * 128, &tmX, kb * 128,
+                                    ti.row0 + b * kDecXBoxRows, fb);
                     filled |= 1u << stage;
-                    if (++stage == C::STAGES) {
+                    if (++stage == nst) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
             int dummy = 0;
-            for (int i = 0; i < C::STAGES; ++i) {
-                const int s = (stage + C::STAGES - 1 - i) % C::STAGES;
+            for (int i = 0; i < nst; ++i) {
+                const int s = (stage + nst - 1 - i) % nst;
                 const uint32_t ph = (s < stage) ? phase : phase ^ 1u;
                 if (filled & (1u << s)) mbar_wait(smem_u32(&full_bar[s]), ph, &dummy, err, kErrTimeoutProducer);
             }
             if (ok) {
-                for (int i = 0; i < C::STAGES; ++i) {
+                for (int i = 0; i < nst; ++i) {
                     if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) break;
-                    if (++stage == C::STAGES) {
+                    if (++stage == nst) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -217,7 +233,7 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                     }
                     mma_commit(smem_u32(&empty_bar[stage]));
                     mma_commit(smem_u32(&tfull_bar[buf]));
-                    if (++stage == C::STAGES) {
+                    if (++stage == nst) {
                         stage = 0;
                         sphase ^= 1u;
                     }
@@ -238,25 +254,25 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
             const int slot = it & 1;
             const uint32_t use = (uint32_t)(it >> 1) & 1u;  // parity of this slot's use
             if (!mbar_wait(smem_u32(&mempty_bar[slot]), use ^ 1u, abort_p, err, kErrTimeoutProducer)) break;
-            float* m = meta + slot * C::META_FLOATS;
+            float* m = meta + slot * M.floats;
             const DecTile ti = decode_dec_tile(tile, s_tiles, s_off, s_cnt, E);
             const uint16_t* bias_e = p.bias + (size_t)ti.e * (GATED ? 2 * p.N_real : p.N_real);
 #pragma unroll
             for (int c = lane; c < (GATED ? 256 : 128); c += 32) {
                 const int n = ti.nt * 128 + (c & 127);
-                m[C::M_BIAS + c] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + (c >> 7) * p.N_real + n)) : 0.f;
+                m[c] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + (c >> 7) * p.N_real + n)) : 0.f;
             }
             const int rtok = min(ti.row0 + lane, p.R - 1);
-            for (int kb = 0; kb < p.KB; ++kb) m[C::M_SA + kb * 32 + lane] = __ldg(p.sa + (size_t)kb * p.R + rtok);
+            for (int kb = 0; kb < p.KB; ++kb) m[M.sa + kb * 32 + lane] = __ldg(p.sa + (size_t)kb * p.R + rtok);
             const float* sw_g = p.sw + ((size_t)ti.e * p.sw_rowblocks + ti.nt) * p.KB;
             for (int kb = lane; kb < p.KB; kb += 32) {
-                m[C::M_SW + kb] = __ldg(sw_g + kb);
-                if (GATED) m[C::M_SW + C::KB_MAX + kb] = __ldg(sw_g + (p.up_rows / 128) * p.KB + kb);
+                m[M.sw + kb] = __ldg(sw_g + kb);
+                if (GATED) m[M.swu + kb] = __ldg(sw_g + (p.up_rows / 128) * p.KB + kb);
             }
             if (!GATED) {
                 const int slot_t = __ldg(p.perm + rtok);
-                reinterpret_cast<int*>(m)[C::M_SLOT + lane] = slot_t;
-                m[C::M_W + lane] = bf16_bits_to_f32(__ldg(p.topk_wb + slot_t));
+                reinterpret_cast<int*>(m)[M.slot + lane] = slot_t;
+                m[M.w + lane] = bf16_bits_to_f32(__ldg(p.topk_wb + slot_t));
             }
             mbar_arrive(smem_u32(&mfull_bar[slot]));
         }
@@ -273,14 +289,14 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
             const uint32_t use = (uint32_t)(it >> 1) & 1u;
             const uint32_t tpar = (uint32_t)it & 1u;
             if (!mbar_wait(smem_u32(&mfull_bar[slot]), use, abort_p, err, kErrTimeoutEpilogue)) break;
-            const float* m = meta + slot * C::META_FLOATS;
+            const float* m = meta + slot * M.floats;
             const DecTile ti = decode_dec_tile(tile, s_tiles, s_off, s_cnt, E);
             const int n = ti.nt * 128 + nl;
             const bool nvalid = n < p.N_real;
             float acc[C::ACC_COLS];
             {
-                const float bg = m[C::M_BIAS + nl];
-                const float bu = GATED ? m[C::M_BIAS + 128 + nl] : 0.f;
+                const float bg = m[nl];
+                const float bu = GATED ? m[128 + nl] : 0.f;
 #pragma unroll
                 for (int j = 0; j < C::BT; ++j) {
                     acc[j] = bg;
@@ -294,10 +310,10 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t tcol = t_lane + (uint32_t)(buf * C::ACC_COLS);
-                const float a = m[C::M_SA + kb * 32 + lane];  // lane j: scale of token j in this K block
-                const float fg = a * m[C::M_SW + kb];
+                const float a = m[M.sa + kb * 32 + lane];  // lane j: scale of token j in this K block
+                const float fg = a * m[M.sw + kb];
                 if (GATED) {
-                    const float fu = a * m[C::M_SW + C::KB_MAX + kb];
+                    const float fu = a * m[M.swu + kb];
                     uint32_t r[64];
                     tmem_ld64(tcol, r);
 #pragma unroll
@@ -341,7 +357,7 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                 const float s_tok = group_scale(amax);  // lane j: scale of token j
                 const float r_tok = recip_rn(s_tok);
                 if (quarter == 0 && lane < ti.rows) p.sh[(size_t)ti.nt * p.R + ti.row0 + lane] = s_tok;
-                if (__all_sync(0xffffffffu, quot_fast(amax))) {
+                if (__all_sync(0xffffffffu, quot_fast(amax) || lane >= ti.rows)) {  // token columns past the tile's rows are never stored
                     const uint32_t k_tok = sign_keep(amax);
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
@@ -358,8 +374,8 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                     if (j + 1 < ti.rows) p.hq[(size_t)(ti.row0 + j + 1) * p.ldq + n] = (uint8_t)(codes >> 8);
                 }
             } else {
-                const int slot_l = reinterpret_cast<const int*>(m)[C::M_SLOT + lane];
-                const float w_l = m[C::M_W + lane];
+                const int slot_l = reinterpret_cast<const int*>(m)[M.slot + lane];
+                const float w_l = m[M.w + lane];
                 mbar_arrive(smem_u32(&mempty_bar[slot]));
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
@@ -379,25 +395,38 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
     }
 }
 
+// The stage ring takes the shared memory the metadata slots and the kernel's
+// static arrays leave, up to `max_stages` stages.
 template <bool GATED>
 static cudaError_t launch_dec(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int grid,
-                              cudaStream_t st) {
+                              int max_stages, cudaStream_t st) {
     using C = DecCfg<GATED>;
-    cudaError_t e = cudaFuncSetAttribute(moe_gemm_decode_kernel<GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncAttributes fa;
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, moe_gemm_decode_kernel<GATED>);
     if (e != cudaSuccess) return e;
-    return launch_pdl(moe_gemm_decode_kernel<GATED>, dim3(grid), dim3(C::THREADS), (size_t)C::SMEM_BYTES, st, tmW,
-                      tmX, p);
+    const size_t meta = (size_t)2 * dec_meta(p.KB).floats * 4;
+    const long long room = (long long)optin - (long long)fa.sharedSizeBytes - 1024 - (long long)meta;
+    int nst = (int)(room / C::STAGE_BYTES);
+    if (nst > max_stages) nst = max_stages;
+    if (nst > C::MAX_STAGES) nst = C::MAX_STAGES;
+    if (nst < 2) return cudaErrorInvalidConfiguration;
+    const size_t smem = (size_t)nst * C::STAGE_BYTES + meta + 1024;
+    e = cudaFuncSetAttribute(moe_gemm_decode_kernel<GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(moe_gemm_decode_kernel<GATED>, dim3(grid), dim3(C::THREADS), smem, st, tmW, tmX, p, nst);
 }
 
 cudaError_t launch_gemm_gateup_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int grid,
                                       cudaStream_t st) {
-    return launch_dec<true>(tmW, tmX, p, grid, st);
+    return launch_dec<true>(tmW, tmX, p, grid, kDecStagesGateUp, st);
 }
 
 cudaError_t launch_gemm_down_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int grid,
                                     cudaStream_t st) {
-    return launch_dec<false>(tmW, tmX, p, grid, st);
+    return launch_dec<false>(tmW, tmX, p, grid, kDecStagesDown, st);
 }
 
 }  // namespace moe

@@ -52,6 +52,16 @@ struct PermuteParams {
     float* sx;    // [Hp/128, R] (K-block-major)
 };
 
+constexpr int kDecXBoxRows = 8;  // activation rows per TMA box of the decode GEMMs
+#ifndef MOE_DEC_STAGES_GATEUP
+#define MOE_DEC_STAGES_GATEUP 5
+#endif
+#ifndef MOE_DEC_STAGES_DOWN
+#define MOE_DEC_STAGES_DOWN 9
+#endif
+constexpr int kDecStagesGateUp = MOE_DEC_STAGES_GATEUP;  // stage ring depth of the decode GEMMs (upper bound)
+constexpr int kDecStagesDown = MOE_DEC_STAGES_DOWN;
+
 struct GemmParams {
     int E, R, KB;          // K / 128
     int N_real;            // gate/up GEMM: I; down GEMM: H
