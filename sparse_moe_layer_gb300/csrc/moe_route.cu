@@ -139,36 +139,6 @@ __device__ __forceinline__ bool last_to_arrive(int* ctr, int total) {
     return s_last != 0;
 }
 
-// ---- thread-block cluster helpers ----
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_id_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-// Every thread of every CTA of the cluster arrives; shared-memory writes made
-// before it are visible to the whole cluster after it.
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// A float from the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
-
 // ---- router: 32 tokens x all experts per cluster, K split over its CTAs ----
 // A cluster of KS CTAs owns a tile of 32 tokens; CTA r of it accumulates the
 // logits of all experts over its own run of 64-wide K chunks on bf16 mma.sync
