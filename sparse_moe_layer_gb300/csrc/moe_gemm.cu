@@ -47,10 +47,10 @@ struct GemmCfg {
     static constexpr int THREADS = (4 + EPI_WARPS) * 32;  // warpgroup 0: producer, MMA, 2 idle warps
     // gate/up: the promotion warps hold 128 accumulators + 32 loaded columns, so
     // warpgroup 0 hands registers to them; the split must not ask for more than
-    // it frees: 8*32*(208-168) = 10240 <= 4*32*(168-72) = 12288
+    // it frees: 8*32*(200-168) = 8192 <= 4*32*(168-88) = 10240
     static constexpr int LAUNCH_REGS = 168;
-    static constexpr int WG0_REGS = 72;
-    static constexpr int EPI_REGS = 208;
+    static constexpr int WG0_REGS = 88;
+    static constexpr int EPI_REGS = 200;
     static constexpr int COLS = BN / 2;  // accumulator columns per epilogue thread
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
     static constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
@@ -103,7 +103,15 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
     __shared__ int abort_flag;
     __shared__ int s_tiles[kMaxExperts + 1], s_off[kMaxExperts + 1], s_cnt[kMaxExperts];
     __shared__ float s_amax[2][2][128];  // [tile parity][column half][row]
-    __shared__ float s_bias[2][C::BN];   // [slot][tile column]: bias of a tile, staged ahead by the metadata warp
+    // staged one tile ahead by the metadata warp, per slot: the tile's bias, the
+    // activation scales of its first two K blocks, the weight scales of those
+    // K blocks (gate: [0..1], up: [2..3]), and for the down GEMM each row's
+    // slot t*k+j and routing weight
+    __shared__ float s_bias[2][C::BN];
+    __shared__ float s_sa01[2][2][128];
+    __shared__ float s_sw01[2][4];
+    __shared__ int s_rslot[2][GATED ? 1 : 128];
+    __shared__ float s_rw[2][GATED ? 1 : 128];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = p.E;
@@ -263,6 +271,23 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 const int n = t.nt * 128 + (c & 127);
                 s_bias[slot][c] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + (c >> 7) * p.N_real + n)) : 0.f;
             }
+            for (int r = lane; r < 128; r += 32) {
+                const int gr = min(t.row0 + r, p.R - 1);
+                s_sa01[slot][0][r] = __ldg(p.sa + gr);
+                s_sa01[slot][1][r] = p.KB > 1 ? __ldg(p.sa + (size_t)p.R + gr) : 0.f;
+                if (!GATED) {
+                    const int st = __ldg(p.perm + gr);
+                    s_rslot[slot][r] = st;
+                    s_rw[slot][r] = bf16_bits_to_f32(__ldg(p.topk_wb + st));
+                }
+            }
+            if (lane < 4) {
+                const float* sw = p.sw + ((size_t)t.e * p.sw_rowblocks + t.nt) * p.KB;
+                const int kb = lane & 1, blk = lane >> 1;  // lanes: g0, g1, u0, u1
+                float v = 0.f;
+                if (kb < p.KB && (GATED || blk == 0)) v = __ldg(sw + (blk ? (p.up_rows / 128) * p.KB : 0) + kb);
+                s_sw01[slot][lane] = v;
+            }
             mbar_arrive(smem_u32(&bfull_bar[slot]));
         }
     } else if (warp >= 4) {
@@ -278,42 +303,9 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
         uint32_t tpar = 0;  // parity of the tiles this CTA has finished
         bool ok = true;
         const int up_off = GATED ? (p.up_rows / 128) * p.KB : 0;  // sw_u = sw_g + up_off
-        // The scales of a tile's first two K blocks are loaded into registers
-        // while the previous tile's epilogue still runs; its bias arrives in
-        // shared memory from the metadata warp.
-        struct Pre {
-            float a0, g0, u0, a1, g1, u1, w;
-            int slot;
-        };
-        auto load_scales = [&](const TileInfo& t) {
-            Pre q{0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0};
-            const int gr = min(t.row0 + row, p.R - 1);
-            if (!GATED) {  // the row's slot and routing weight, used by the epilogue
-                q.slot = __ldg(p.perm + gr);
-                q.w = bf16_bits_to_f32(__ldg(p.topk_wb + q.slot));
-            }
-            const float* sw = p.sw + ((size_t)t.e * p.sw_rowblocks + t.nt) * p.KB;
-            q.a0 = __ldg(p.sa + gr);
-            q.g0 = __ldg(sw);
-            if (GATED) q.u0 = __ldg(sw + up_off);
-            if (p.KB > 1) {
-                q.a1 = __ldg(p.sa + (size_t)p.R + gr);
-                q.g1 = __ldg(sw + 1);
-                if (GATED) q.u1 = __ldg(sw + up_off + 1);
-            }
-            return q;
-        };
-        TileInfo nxt{};
-        Pre pre{0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0};
-        if (blockIdx.x < total) {
-            nxt = decode_tile(blockIdx.x, s_tiles, s_off, s_cnt, E);
-            pre = load_scales(nxt);
-        }
         int tcount = 0;
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, tpar ^= 1u, ++tcount) {
-            const TileInfo ti = nxt;
-            const int my_slot = pre.slot;
-            const float my_w = pre.w;
+            const TileInfo ti = decode_tile(tile, s_tiles, s_off, s_cnt, E);
             const int grow = ti.row0 + row;
             const bool valid = row < ti.rows;
             const int grow_c = min(grow, p.R - 1);
@@ -327,6 +319,11 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 acc[i] = s_bias[bslot][64 * half + i];
                 if (GATED) acc[64 + i] = s_bias[bslot][128 + 64 * half + i];
             }
+            // scales of K blocks 0 and 1 (later ones are loaded two K blocks ahead)
+            float a0 = s_sa01[bslot][0][row], a1 = s_sa01[bslot][1][row];
+            float g0 = s_sw01[bslot][0], g1 = s_sw01[bslot][1], u0 = s_sw01[bslot][2], u1 = s_sw01[bslot][3];
+            const int my_slot = GATED ? 0 : s_rslot[bslot][GATED ? 0 : row];
+            const float my_w = GATED ? 0.f : s_rw[bslot][GATED ? 0 : row];
             mbar_arrive(smem_u32(&bempty_bar[bslot]));
             const float* sa_row = p.sa + grow_c;  // element kb at sa_row[kb * R]
             const float* sw_g = p.sw + ((size_t)ti.e * p.sw_rowblocks + ti.nt) * p.KB;
@@ -335,7 +332,6 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             const bool active = quarter * 32 < ti.rows;
             // scales of K blocks kb and kb+1 are in registers; kb+2 is loaded
             // while kb is promoted, so no K block waits on a global load
-            float a0 = pre.a0, g0 = pre.g0, u0 = pre.u0, a1 = pre.a1, g1 = pre.g1, u1 = pre.u1;
             for (int kb = 0; kb < p.KB; ++kb) {
                 float a2 = 0.f, g2 = 0.f, u2 = 0.f;
                 if (active && kb + 2 < p.KB) {
@@ -375,10 +371,6 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 a1 = a2; g1 = g2; u1 = u2;
             }
             if (!ok) break;
-            if (tile + (int)gridDim.x < total) {
-                nxt = decode_tile(tile + gridDim.x, s_tiles, s_off, s_cnt, E);
-                pre = load_scales(nxt);
-            }
 
             if (GATED) {
                 // h = silu(g) * u for this thread's 64 columns of the 128-wide group
