@@ -29,20 +29,20 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-GATEUP_LAUNCH_REGS = 168  # must match GemmCfg<true>::LAUNCH_REGS (setmaxnreg budget)
+GEMM_LAUNCH_REGS = 168  # must match GemmCfg<...>::LAUNCH_REGS (setmaxnreg budget)
 
 
-def _check_gateup_registers(log_path: str) -> None:
-    """The gate/up GEMM moves registers between warpgroups with setmaxnreg; the
-    split balances only if the kernel launches with exactly 168 registers."""
+def _check_gemm_registers(log_path: str) -> None:
+    """The prefill GEMMs move registers between warpgroups with setmaxnreg; the
+    split balances only if each kernel launches with exactly 168 registers."""
     import re
     text = open(log_path).read()
-    m = re.search(r"Compiling entry function '(_ZN3moe15moe_gemm_kernelILb1E[^']*)'.*?Used (\d+) registers", text, re.S)
-    if not m or int(m.group(2)) != GATEUP_LAUNCH_REGS:
-        got = m.group(2) if m else "?"
-        raise RuntimeError(f"gate/up GEMM compiled to {got} registers, expected {GATEUP_LAUNCH_REGS}")
+    found = re.findall(r"Compiling entry function '(_ZN3moe15moe_gemm_kernelILb[01]E[^']*)'.*?Used (\d+) registers", text,
+                       re.S)
+    if len(found) != 2 or any(int(n) != GEMM_LAUNCH_REGS for _, n in found):
+        raise RuntimeError(f"prefill GEMMs compiled to {[n for _, n in found]} registers, expected {GEMM_LAUNCH_REGS}")
     if "setmaxnreg" in text and "ignored" in text:
-        raise RuntimeError("ptxas ignored setmaxnreg in the gate/up GEMM")
+        raise RuntimeError("ptxas ignored setmaxnreg in a prefill GEMM")
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -63,7 +63,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    _check_gateup_registers(os.path.join(BUILD, "moe_gemm.cu.log"))
+    _check_gemm_registers(os.path.join(BUILD, "moe_gemm.cu.log"))
     tmp = LIB + ".tmp"
     r = subprocess.run([nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", tmp, *objs],
                        capture_output=True, text=True)

@@ -179,11 +179,13 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     rp.E = E;
     rp.k = top_k;
     rp.nchunks = nch;
-    rp.nt1 = Ip / 128;
-    rp.nt2 = Hp / 128;
-    // Few rows per expert (decode): weight-streaming kernels with 32-row token tiles.
+    // Few rows per expert (decode): weight-streaming kernels with 32-row token
+    // tiles and 128-feature n-tiles; else 128-row tiles of 128 h features
+    // (gate/up) or 256 output features (down: two w2 blocks per tile).
     const bool decode = (long long)R <= 64LL * E;
     rp.bm = decode ? 32 : 128;
+    rp.nt1 = Ip / 128;
+    rp.nt2 = decode ? Hp / 128 : (Hp / 128 + 1) / 2;
     rp.topk_idx = reinterpret_cast<int32_t*>(ws + L.topk_idx);
     rp.topk_w = reinterpret_cast<float*>(ws + L.topk_w);
     rp.topk_wb = reinterpret_cast<uint16_t*>(ws + L.topk_wb);
@@ -286,7 +288,7 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     g2.part = reinterpret_cast<float*>(ws + L.part);
     g2.ldp = Hp;
     g2.status = rp.status;
-    long long t2 = mt_bound * (Hp / 128);
+    long long t2 = mt_bound * rp.nt2;
     int grid2 = (int)(t2 < sms ? t2 : sms);
     if ((decode ? launch_gemm_down_decode(tmB2, tmA2, g2, grid2, st) : launch_gemm_down(tmA2, tmB2, g2, grid2, st)) !=
         cudaSuccess)

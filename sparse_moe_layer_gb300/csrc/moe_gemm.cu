@@ -37,11 +37,13 @@ namespace moe {
 template <bool GATED>
 struct GemmCfg {
     static constexpr int BM = 128;
-    static constexpr int BN = GATED ? 256 : 128;  // gate/up: 128 gate + 128 up columns of one h block
+    // two 128-row weight blocks per tile, one N=256 MMA per K step: gate/up the
+    // gate and the up block of one h block, down two consecutive w2 blocks
+    static constexpr int BN = 256;
     static constexpr int A_BYTES = BM * 128;
     static constexpr int B_BYTES = BN * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = GATED ? 4 : 6;
+    static constexpr int STAGES = 4;
     static constexpr int NBUF = 512 / BN;  // TMEM partial buffers (all 512 columns)
     static constexpr int EPI_WARPS = 8;                   // warpgroups 1 and 2
     static constexpr int THREADS = (4 + EPI_WARPS) * 32;  // warpgroup 0: producer, MMA, 2 idle warps
@@ -60,6 +62,15 @@ struct GemmCfg {
 struct TileInfo {
     int e, nt, row0, rows;
 };
+
+// Row block (of the expert's weight matrix) of a tile's block `which` (0/1):
+// gate/up: the gate block and the up block of h block nt; down: blocks 2nt and
+// 2nt+1, the second past the last one (== RB) when RB is odd -- it is then
+// loaded as zeros or another expert's block and its results are dropped.
+template <bool GATED>
+__device__ __forceinline__ int weight_block(const GemmParams& p, int nt, int which) {
+    return GATED ? (which ? p.up_rows / 128 + nt : nt) : 2 * nt + which;
+}
 
 
 __device__ __forceinline__ TileInfo decode_tile(int tile, const int* s_tiles, const int* s_off, const int* s_cnt,
@@ -159,7 +170,7 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
     pdl_allow_dependents();
 
     if (warp < 4) {
-        if (GATED) regs_release<C::WG0_REGS>();
+        regs_release<C::WG0_REGS>();
     }
     if (warp == 0) {
         if (lane == 0) {
@@ -168,11 +179,11 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             uint32_t phase = 0;
             uint32_t filled = 0;  // bit s: stage s was filled at least once
             bool ok = true;
-            const int ublk = GATED ? (p.up_rows / 128) * p.KB : 0;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const TileInfo ti = decode_tile(tile, s_tiles, s_off, s_cnt, E);
                 // blocked weights: block (e, row block, kb) starts at row ((e*RB + rb)*KB + kb)*128
-                const int bblk = (ti.e * p.sw_rowblocks + ti.nt) * p.KB;
+                const int blk0 = (ti.e * p.sw_rowblocks + weight_block<GATED>(p, ti.nt, 0)) * p.KB;
+                const int blk1 = (ti.e * p.sw_rowblocks + weight_block<GATED>(p, ti.nt, 1)) * p.KB;
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) {
                         ok = false;
@@ -183,8 +194,8 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                     const uint32_t a_dst = smem_u32(smem + stage * C::STAGE_BYTES);
                     const uint32_t b_dst = a_dst + C::A_BYTES;
                     tma_load_2d(a_dst, &tmA, kb * 128, ti.row0, fb);
-                    tma_load_2d(b_dst, &tmB, 0, (bblk + kb) * 128, fb);
-                    if (GATED) tma_load_2d(b_dst + 128 * 128, &tmB, 0, (bblk + ublk + kb) * 128, fb);
+                    tma_load_2d(b_dst, &tmB, 0, (blk0 + kb) * 128, fb);
+                    tma_load_2d(b_dst + 128 * 128, &tmB, 0, (blk1 + kb) * 128, fb);
                     filled |= 1u << stage;
                     if (++stage == C::STAGES) {
                         stage = 0;
@@ -268,8 +279,11 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             const TileInfo t = decode_tile(tile, s_tiles, s_off, s_cnt, E);
             const uint16_t* bias_e = p.bias + (size_t)t.e * (GATED ? 2 * p.N_real : p.N_real);
             for (int c = lane; c < C::BN; c += 32) {
-                const int n = t.nt * 128 + (c & 127);
-                s_bias[slot][c] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + (c >> 7) * p.N_real + n)) : 0.f;
+                // gate/up: h feature nt*128 + c%128 of the gate (c < 128) or up half of b13;
+                // down: output feature (2nt + c/128)*128 + c%128
+                const int n = (GATED ? t.nt : 2 * t.nt + (c >> 7)) * 128 + (c & 127);
+                s_bias[slot][c] =
+                    n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + (GATED ? (c >> 7) * p.N_real : 0) + n)) : 0.f;
             }
             for (int r = lane; r < 128; r += 32) {
                 const int gr = min(t.row0 + r, p.R - 1);
@@ -282,17 +296,17 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 }
             }
             if (lane < 4) {
-                const float* sw = p.sw + ((size_t)t.e * p.sw_rowblocks + t.nt) * p.KB;
-                const int kb = lane & 1, blk = lane >> 1;  // lanes: g0, g1, u0, u1
+                const int kb = lane & 1, which = lane >> 1;  // lanes: block 0 kb 0, 1; block 1 kb 0, 1
+                const int b = weight_block<GATED>(p, t.nt, which);
                 float v = 0.f;
-                if (kb < p.KB && (GATED || blk == 0)) v = __ldg(sw + (blk ? (p.up_rows / 128) * p.KB : 0) + kb);
+                if (kb < p.KB && b < p.sw_rowblocks) v = __ldg(p.sw + ((size_t)t.e * p.sw_rowblocks + b) * p.KB + kb);
                 s_sw01[slot][lane] = v;
             }
             mbar_arrive(smem_u32(&bfull_bar[slot]));
         }
     } else if (warp >= 4) {
         // -------------------------------------------- promotion + epilogue
-        if (GATED) regs_acquire<C::EPI_REGS>();
+        regs_acquire<C::EPI_REGS>();
         const int ew = warp - 4;
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int half = ew >> 2;      // which half of the columns
@@ -302,7 +316,6 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
         uint32_t tphase = 0;
         uint32_t tpar = 0;  // parity of the tiles this CTA has finished
         bool ok = true;
-        const int up_off = GATED ? (p.up_rows / 128) * p.KB : 0;  // sw_u = sw_g + up_off
         int tcount = 0;
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, tpar ^= 1u, ++tcount) {
             const TileInfo ti = decode_tile(tile, s_tiles, s_off, s_cnt, E);
@@ -317,7 +330,7 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
                 acc[i] = s_bias[bslot][64 * half + i];
-                if (GATED) acc[64 + i] = s_bias[bslot][128 + 64 * half + i];
+                acc[64 + i] = s_bias[bslot][128 + 64 * half + i];
             }
             // scales of K blocks 0 and 1 (later ones are loaded two K blocks ahead)
             float a0 = s_sa01[bslot][0][row], a1 = s_sa01[bslot][1][row];
@@ -326,7 +339,10 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             const float my_w = GATED ? 0.f : s_rw[bslot][GATED ? 0 : row];
             mbar_arrive(smem_u32(&bempty_bar[bslot]));
             const float* sa_row = p.sa + grow_c;  // element kb at sa_row[kb * R]
-            const float* sw_g = p.sw + ((size_t)ti.e * p.sw_rowblocks + ti.nt) * p.KB;
+            const int b1 = weight_block<GATED>(p, ti.nt, 1);
+            const bool has1 = b1 < p.sw_rowblocks;  // down GEMM, odd block count: the last tile has one block
+            const float* sw0 = p.sw + ((size_t)ti.e * p.sw_rowblocks + weight_block<GATED>(p, ti.nt, 0)) * p.KB;
+            const float* sw1 = p.sw + ((size_t)ti.e * p.sw_rowblocks + b1) * p.KB;
             // Warps whose TMEM lane quarter holds no valid row of this tile only
             // keep the buffer hand-over going (decode tiles have few rows).
             const bool active = quarter * 32 < ti.rows;
@@ -336,8 +352,8 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 float a2 = 0.f, g2 = 0.f, u2 = 0.f;
                 if (active && kb + 2 < p.KB) {
                     a2 = __ldg(sa_row + (size_t)(kb + 2) * p.R);
-                    g2 = __ldg(sw_g + kb + 2);
-                    if (GATED) u2 = __ldg(sw_g + up_off + kb + 2);
+                    g2 = __ldg(sw0 + kb + 2);
+                    if (has1) u2 = __ldg(sw1 + kb + 2);
                 }
                 if (!mbar_wait(smem_u32(&tfull_bar[buf]), tphase, abort_p, err, kErrTimeoutEpilogue)) {
                     ok = false;
@@ -410,10 +426,16 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
             } else {
                 if (valid) {
                     const float w = my_w;
-                    float4* dst = reinterpret_cast<float4*>(p.part + (size_t)my_slot * p.ldp + n0);
 #pragma unroll
-                    for (int v = 0; v < 16; ++v)
-                        dst[v] = make_float4(w * acc[4 * v], w * acc[4 * v + 1], w * acc[4 * v + 2], w * acc[4 * v + 3]);
+                    for (int b = 0; b < 2; ++b) {
+                        if (b == 1 && !has1) break;
+                        float4* dst =
+                            reinterpret_cast<float4*>(p.part + (size_t)my_slot * p.ldp + (2 * ti.nt + b) * 128 + 64 * half);
+#pragma unroll
+                        for (int v = 0; v < 16; ++v)
+                            dst[v] = make_float4(w * acc[64 * b + 4 * v], w * acc[64 * b + 4 * v + 1],
+                                                 w * acc[64 * b + 4 * v + 2], w * acc[64 * b + 4 * v + 3]);
+                    }
                 }
             }
         }
@@ -431,7 +453,7 @@ template <bool GATED>
 static cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
                                cudaStream_t st) {
     using C = GemmCfg<GATED>;
-    if (GATED) {
+    {
         // the register hand-over between warpgroups balances only at this launch count
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, moe_gemm_kernel<GATED>);

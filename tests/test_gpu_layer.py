@@ -61,10 +61,12 @@ def full_check(moe, layer: Layer, n_sample: int | None = None):
         assert np.array_equal(v[key].cpu().numpy(), p[key]), key
     # GEMM tile lists cover every expert's rows
     st = v["status"].cpu().numpy()
-    bm = 32 if T * k <= 64 * E else 128  # decode-sized batches use 32-row token tiles
+    decode = T * k <= 64 * E  # decode-sized batches: 32-row token tiles, 128-feature n-tiles
+    bm = 32 if decode else 128
     assert st[3] == bm
     mt = (p["count"] + bm - 1) // bm
-    assert st[1] == mt.sum() * (layer.Ip // 128) and st[2] == mt.sum() * (layer.Hp // 128)
+    nt2 = layer.Hp // 128 if decode else (layer.Hp // 128 + 1) // 2  # prefill down GEMM: 256-feature tiles
+    assert st[1] == mt.sum() * (layer.Ip // 128) and st[2] == mt.sum() * nt2
     # x quantisation: bit-exact codes and scales in every permuted row
     xq, sx = oracle.quant_rows_bf16(layer.x)
     tok_of_row = p["perm"] // k
