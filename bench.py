@@ -169,39 +169,54 @@ def build_layer(cfg, device):
     return layer, bf16(x), x
 
 
-def cpu_oracle_leg(cfg, n_units: int, steps: int = 1):
-    """Time the oracle (single thread) on a bounded sample of the workload.
-
-    A unit is one (token, slot) expert evaluation: 1/top_k of a token.  Returns
-    (tokens per second, sample description, seconds)."""
+def cpu_oracle_leg(cfg, seconds: float):
+    """Time the oracle (single thread) on a bounded sample of the workload:
+    about `seconds` of CPU work -- the tokens of a fixed random sample (at most
+    the whole batch), the full layer per token, repeated if one pass is short.
+    Returns (tokens per second, sample description, seconds)."""
     import oracle
     x = synth.layer_x(cfg)
     rw, rb = synth.router(cfg)
     b13, b2 = synth.expert_biases(cfg)
     k = cfg.top_k
-    n_tok = max(1, -(-n_units // k))
-    rng = np.random.default_rng(1234)
-    tokens = np.sort(rng.choice(cfg.T, size=min(n_tok, cfg.T), replace=False)).astype(np.int32)
-    r = oracle.router(np.ascontiguousarray(x[tokens]), rw, rb, k)
-    needed = np.unique(r["idx"])
+    order = np.random.default_rng(1234).permutation(cfg.T).astype(np.int32)
     E, Hp, Ip = cfg.E, cfg.Hp, cfg.Ip
     q13 = np.zeros((E, 2 * Ip, Hp), np.uint8)
     s13 = np.ones((E, 2 * Ip // 128, Hp // 128), np.float32)
     q2 = np.zeros((E, Hp, Ip), np.uint8)
     s2 = np.ones((E, Hp // 128, Ip // 128), np.float32)
+    packed = set()
     from concurrent.futures import ThreadPoolExecutor
 
-    def pack(e):  # weight conversion is offline for both sides: untimed
-        oracle.pack_w13(synth.w13_master(cfg, int(e), 1), q13[e:e + 1], s13[e:e + 1])
-        oracle.pack_w2(synth.w2_master(cfg, int(e), 1), q2[e:e + 1], s2[e:e + 1])
+    def pack_for(tokens):  # weight conversion is offline for both sides: untimed
+        r = oracle.router(np.ascontiguousarray(x[tokens]), rw, rb, k)
+        todo = [int(e) for e in np.unique(r["idx"]) if int(e) not in packed]
 
-    with ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
-        list(ex.map(pack, needed))
+        def pack(e):
+            oracle.pack_w13(synth.w13_master(cfg, e, 1), q13[e:e + 1], s13[e:e + 1])
+            oracle.pack_w2(synth.w2_master(cfg, e, 1), q2[e:e + 1], s2[e:e + 1])
+
+        with ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
+            list(ex.map(pack, todo))
+        packed.update(todo)
+
+    # calibrate on a few tokens, then size the sample to the time budget
+    probe = np.sort(order[:min(2, cfg.T)])
+    pack_for(probe)
     t0 = time.perf_counter()
-    for _ in range(steps):
+    oracle.forward(x, rw, rb, q13, s13, b13, q2, s2, b2, k, tokens=probe)
+    per_token = max((time.perf_counter() - t0) / len(probe), 1e-6)
+    n = int(min(cfg.T, max(1, seconds / per_token)))
+    passes = max(1, int(seconds / (n * per_token)))
+    tokens = np.sort(order[:n])
+    pack_for(tokens)
+    t0 = time.perf_counter()
+    for _ in range(passes):
         oracle.forward(x, rw, rb, q13, s13, b13, q2, s2, b2, k, tokens=tokens)
     dt = time.perf_counter() - t0
-    return steps * len(tokens) / dt, f"{len(tokens)} of {cfg.T} tokens ({len(needed)} experts), full layer per token", dt
+    desc = (f"{n} of {cfg.T} tokens x {passes} pass(es) ({len(packed)} experts), full layer per token, "
+            f"single-threaded fp64 oracle")
+    return passes * n / dt, desc, dt
 
 
 def run_reference(args, cfg, rank):
@@ -259,7 +274,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=[c.name for c in synth.CONFIGS])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-units", type=int, default=32, help="(token, slot) units in the CPU-oracle sample")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work in the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -423,7 +438,7 @@ def main():
                 gpu_launches=5 * K,
                 clocks=sampler.summary())
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, desc, dt = cpu_oracle_leg(cfg, args.cpu_units)
+        v, desc, dt = cpu_oracle_leg(cfg, args.cpu_seconds)
         line["cpu_baseline"] = dict(value=v, unit="tokens/s", cores=1, kind="oracle", sample=desc, seconds=dt)
     if rank == 0:
         print(json.dumps(line), flush=True)
