@@ -17,6 +17,7 @@ value = tokens of all ranks / max-over-ranks time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -141,7 +142,19 @@ class ClockSampler:
         return dict(sm_mhz=statistics.median(loaded), sm_max_mhz=mx, reasons=sorted(reasons), samples=len(sm))
 
 
-def build_layer(cfg, device):
+def one_per_expert_inputs(cfg):
+    """x and router of a batch that sends exactly one row to every expert
+    (T = E / top_k): token t's logit is 1 for experts [t*k, t*k+k) and 0 else
+    (x[t] = e_t, router_w[e] = e_{e//k}, router_b = 0), bf16 bits."""
+    one = np.uint16(0x3F80)  # bf16 1.0
+    x = np.zeros((cfg.T, cfg.H), np.uint16)
+    x[np.arange(cfg.T), np.arange(cfg.T)] = one
+    rw = np.zeros((cfg.E, cfg.H), np.uint16)
+    rw[np.arange(cfg.E), np.arange(cfg.E) // cfg.top_k] = one
+    return x, rw, np.zeros(cfg.E, np.uint16)
+
+
+def build_layer(cfg, device, routing="synthetic"):
     """Inputs of the workload resident on the device; weights packed by the library."""
     import torch
     import sparse_moe_layer_gb300 as moe
@@ -149,8 +162,11 @@ def build_layer(cfg, device):
     def bf16(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
 
-    x = synth.layer_x(cfg)
-    rw, rb = synth.router(cfg)
+    if routing == "one_per_expert":
+        x, rw, rb = one_per_expert_inputs(cfg)
+    else:
+        x = synth.layer_x(cfg)
+        rw, rb = synth.router(cfg)
     b13, b2 = synth.expert_biases(cfg)
     E, H, I, Hp, Ip = cfg.E, cfg.H, cfg.I, cfg.Hp, cfg.Ip
     w13 = torch.empty(moe.w13_shape(E, H, I), dtype=torch.uint8, device=device)
@@ -276,10 +292,20 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work in the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="batch size T instead of the workload's (small-batch decode sweep; same weights)")
+    ap.add_argument("--routing", default="synthetic", choices=["synthetic", "one_per_expert"],
+                    help="one_per_expert: T = E/top_k tokens routed so that every expert gets exactly one row")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     cfg = synth.config(args.config)
+    if args.routing == "one_per_expert":
+        if cfg.E % cfg.top_k or cfg.E // cfg.top_k > cfg.H:
+            ap.error("one_per_expert needs top_k | E and E/top_k <= H")
+        cfg = dataclasses.replace(cfg, T=cfg.E // cfg.top_k)
+    elif args.tokens:
+        cfg = dataclasses.replace(cfg, T=args.tokens)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -300,7 +326,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    layer, x_dev, x_host_np = build_layer(cfg, dev)
+    layer, x_dev, x_host_np = build_layer(cfg, dev, args.routing)
     T, H = cfg.T, cfg.H
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -423,7 +449,9 @@ def main():
     line = dict(metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=K, warmup=args.warmup,
                 ms_per_step=ms, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="e4m3",
                 data="synthetic",
-                config=dict(workload=workload_str(cfg), parallelism=f"replicas{world}",
+                config=dict(workload=workload_str(cfg) + ("" if args.routing == "synthetic" else
+                                                          " routing=one row per expert (T = E/top_k)"),
+                            parallelism=f"replicas{world}",
                             l2="flushed before every step (256 MiB write, outside the timed events)",
                             weights="FP8 e4m3 128x128 block scales, packed on device by moe_pack_weights"),
                 roofline=roof,

@@ -149,7 +149,8 @@ def margin_attempts(cfg: LayerConfig) -> np.ndarray:
         raise KeyError(f"no redraw table for {cfg.name}; regenerate tests/golden/margin_redraws.json")
     att = np.zeros(cfg.T, np.uint32)
     for t, a in table[cfg.name].items():
-        att[int(t)] = a
+        if int(t) < cfg.T:  # a shape with fewer tokens uses a prefix of the rows
+            att[int(t)] = a
     return att
 
 
