@@ -439,3 +439,174 @@ void oracle_forward(const uint16_t* x, const uint16_t* rw, const uint16_t* rb, c
     free(y);
     free(acc);
 }
+
+/* ------------------------------------------------------------------ */
+/* MXFP8 variant                                                      */
+/* ------------------------------------------------------------------ */
+/* "Hosting Qwen on Blackwell" (section "Quantization"): on Blackwell the
+ * throughput case for FP8 is microscaling, one power-of-two scale per 32
+ * consecutive values.  The scale is the one the OCP Microscaling Formats
+ * (MX) specification v1.0 (section 6.3) defines: for a group of 32 values,
+ * X = floor(log2(max |v|)) - 8 (8 = the exponent of e4m3's largest normal,
+ * 448 = 1.75 * 2^8), kept as the UE8M0 byte X + 127; the codes are
+ * e4m3(v / 2^X) -- nearest, ties to even, saturating to +-448 (values of the
+ * top binade above 448 saturate, as the specification allows).  Readings
+ * where that is silent (also in the design notes): an all-zero group gets the
+ * byte 0 (2^-127) and +0 codes; X is clamped to [-127, 127]; the layer is the
+ * same pipeline as the 128x128 variant with every quantiser replaced by this
+ * one (x along H, h along I, weight rows along K), padding to multiples of
+ * 128 as there. */
+static uint8_t mx_group(const float* v, int n, uint8_t* q) {
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = fabsf(v[i]);
+        if (a > amax) amax = a;
+    }
+    for (int i = 0; i < 32; ++i) q[i] = 0;
+    if (amax == 0.0f) return 0;
+    int e;
+    frexp((double)amax, &e); /* amax = f * 2^e, f in [0.5, 1): floor(log2(amax)) = e - 1 */
+    int X = e - 1 - 8;
+    if (X < -127) X = -127;
+    if (X > 127) X = 127;
+    for (int i = 0; i < n; ++i) q[i] = oracle_e4m3_encode((float)ldexp((double)v[i], -X));
+    return (uint8_t)(X + 127);
+}
+
+/* MX quantisation of `rows` rows of `cols` fp32 values: codes [rows, Cp] and
+ * scale bytes [rows, Cp/32], Cp = cols padded to a multiple of 128. */
+void oracle_mx_quant_rows_f32(const float* x, int rows, int cols, uint8_t* q, uint8_t* s) {
+    int Cp = (cols + 127) / 128 * 128;
+    for (int r = 0; r < rows; ++r)
+        for (int g = 0; g < Cp / 32; ++g) {
+            int c0 = g * 32;
+            int n = cols - c0 < 32 ? (cols - c0 > 0 ? cols - c0 : 0) : 32;
+            s[(size_t)r * (Cp / 32) + g] = mx_group(x + (size_t)r * cols + c0, n, q + (size_t)r * Cp + c0);
+        }
+}
+
+void oracle_mx_quant_rows_bf16(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* s) {
+    float* f = (float*)malloc(sizeof(float) * (size_t)rows * cols);
+    for (size_t i = 0; i < (size_t)rows * cols; ++i) f[i] = (float)bf16_value(x[i]);
+    oracle_mx_quant_rows_f32(f, rows, cols, q, s);
+    free(f);
+}
+
+/* Weights: every output row quantised along K.  w13 [n_exp, 2I, H] ->
+ * q [n_exp, 2Ip, Hp] (gate rows [0,I), up rows [Ip, Ip+I), pad rows 0),
+ * s [n_exp, 2Ip, Hp/32]; w2 [n_exp, H, I] -> q [n_exp, Hp, Ip],
+ * s [n_exp, Hp, Ip/32].  Pad rows have the byte 0 and codes 0. */
+static void mx_pack(const float* w, int rows, int cols, int rows_p, int cols_p, const int* row_map, uint8_t* q,
+                    uint8_t* s) {
+    memset(q, 0, (size_t)rows_p * cols_p);
+    memset(s, 0, (size_t)rows_p * (cols_p / 32));
+    uint8_t* qr = (uint8_t*)malloc((size_t)cols_p);
+    uint8_t* sr = (uint8_t*)malloc((size_t)cols_p / 32);
+    for (int r = 0; r < rows; ++r) {
+        oracle_mx_quant_rows_f32(w + (size_t)r * cols, 1, cols, qr, sr);
+        int d = row_map ? row_map[r] : r;
+        memcpy(q + (size_t)d * cols_p, qr, (size_t)cols_p);
+        memcpy(s + (size_t)d * (cols_p / 32), sr, (size_t)cols_p / 32);
+    }
+    free(qr);
+    free(sr);
+}
+
+void oracle_mx_pack_w13(const float* w13, int H, int I, int n_exp, uint8_t* q, uint8_t* s) {
+    int Hp = (H + 127) / 128 * 128, Ip = (I + 127) / 128 * 128;
+    int* map = (int*)malloc(sizeof(int) * 2 * (size_t)I);
+    for (int r = 0; r < I; ++r) {
+        map[r] = r;
+        map[I + r] = Ip + r;
+    }
+    for (int e = 0; e < n_exp; ++e)
+        mx_pack(w13 + (size_t)e * 2 * I * H, 2 * I, H, 2 * Ip, Hp, map, q + (size_t)e * 2 * Ip * Hp,
+                s + (size_t)e * 2 * Ip * (Hp / 32));
+    free(map);
+}
+
+void oracle_mx_pack_w2(const float* w2, int H, int I, int n_exp, uint8_t* q, uint8_t* s) {
+    int Hp = (H + 127) / 128 * 128, Ip = (I + 127) / 128 * 128;
+    for (int e = 0; e < n_exp; ++e)
+        mx_pack(w2 + (size_t)e * H * I, H, I, Hp, Ip, NULL, q + (size_t)e * Hp * Ip, s + (size_t)e * Hp * (Ip / 32));
+}
+
+/* sum over 32-groups g of 2^(sa[g]-127) * 2^(sw[n,g]-127) * sum_{i in g}
+ * dec(a[i]) * dec(w[n,i]), in fp64 (exact: e4m3 products and their sums over
+ * 32 fit in fp64, the scales are powers of two). */
+static double mx_dot(const uint8_t* a, const uint8_t* sa, const uint8_t* w, const uint8_t* sw, int n, int Kp) {
+    int G = Kp / 32;
+    double acc = 0.0;
+    for (int g = 0; g < G; ++g) {
+        double part = 0.0;
+        for (int i = g * 32; i < g * 32 + 32; ++i) part += E4M3[a[i]] * E4M3[w[(size_t)n * Kp + i]];
+        acc += ldexp(part, ((int)sa[g] - 127) + ((int)sw[(size_t)n * G + g] - 127));
+    }
+    return acc;
+}
+
+static void mx_expert_ffn(const uint8_t* xq, const uint8_t* sx, const uint8_t* w13e, const uint8_t* s13e,
+                          const uint16_t* b13e, const uint8_t* w2e, const uint8_t* s2e, const uint16_t* b2e, int H,
+                          int I, uint8_t* hq, uint8_t* sh, double* y) {
+    int Hp = (H + 127) / 128 * 128, Ip = (I + 127) / 128 * 128;
+    float* h = (float*)malloc(sizeof(float) * (size_t)I);
+    for (int n = 0; n < I; ++n) {
+        double g = (double)bf16_value(b13e[n]) + mx_dot(xq, sx, w13e, s13e, n, Hp);
+        double u = (double)bf16_value(b13e[I + n]) + mx_dot(xq, sx, w13e, s13e, Ip + n, Hp);
+        double silu = g / (1.0 + exp(-g));
+        h[n] = (float)(silu * u);
+    }
+    oracle_mx_quant_rows_f32(h, 1, I, hq, sh);
+    free(h);
+    for (int n = 0; n < H; ++n) y[n] = (double)bf16_value(b2e[n]) + mx_dot(hq, sh, w2e, s2e, n, Ip);
+}
+
+/* The layer with MXFP8 quantisation; arguments as oracle_forward, with the
+ * scale arrays in UE8M0 bytes (s13 [E, 2Ip, Hp/32], s2 [E, Hp, Ip/32]) and
+ * sh_rows [ntok*k, Ip/32]. */
+void oracle_mx_forward(const uint16_t* x, const uint16_t* rw, const uint16_t* rb, const uint8_t* w13,
+                       const uint8_t* s13, const uint16_t* b13, const uint8_t* w2, const uint8_t* s2,
+                       const uint16_t* b2, int T, int H, int I, int E, int k, const int32_t* tokens, int ntok,
+                       uint16_t* out_rows, uint8_t* hq_rows, uint8_t* sh_rows, double* y_rows, int32_t* idx_rows) {
+    e4m3_init();
+    int Hp = (H + 127) / 128 * 128, Ip = (I + 127) / 128 * 128;
+    if (!tokens) ntok = T;
+    double* logits = (double*)malloc(sizeof(double) * (size_t)E);
+    uint8_t* xq = (uint8_t*)malloc((size_t)Hp);
+    uint8_t* sx = (uint8_t*)malloc((size_t)Hp / 32);
+    uint8_t* hq = (uint8_t*)malloc((size_t)Ip);
+    uint8_t* sh = (uint8_t*)malloc((size_t)Ip / 32);
+    double* y = (double*)malloc(sizeof(double) * (size_t)H);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+    int32_t idx[64];
+    float wf[64];
+    uint16_t wb[64];
+    for (int i = 0; i < ntok; ++i) {
+        int t = tokens ? tokens[i] : i;
+        const uint16_t* xt = x + (size_t)t * H;
+        route_token(xt, rw, rb, H, E, k, idx, wf, wb, logits, NULL);
+        oracle_mx_quant_rows_bf16(xt, 1, H, xq, sx);
+        for (int n = 0; n < H; ++n) acc[n] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int e = idx[j];
+            mx_expert_ffn(xq, sx, w13 + (size_t)e * 2 * Ip * Hp, s13 + (size_t)e * 2 * Ip * (Hp / 32),
+                          b13 + (size_t)e * 2 * I, w2 + (size_t)e * Hp * Ip, s2 + (size_t)e * Hp * (Ip / 32),
+                          b2 + (size_t)e * H, H, I, hq, sh, y);
+            double wj = bf16_value(wb[j]);
+            for (int n = 0; n < H; ++n) acc[n] += wj * y[n];
+            size_t row = (size_t)i * k + j;
+            if (hq_rows) memcpy(hq_rows + row * Ip, hq, (size_t)Ip);
+            if (sh_rows) memcpy(sh_rows + row * (Ip / 32), sh, (size_t)Ip / 32);
+            if (y_rows) memcpy(y_rows + row * H, y, sizeof(double) * (size_t)H);
+            if (idx_rows) idx_rows[row] = e;
+        }
+        for (int n = 0; n < H; ++n) out_rows[(size_t)i * H + n] = oracle_bf16_from_f64(acc[n]);
+    }
+    free(logits);
+    free(xq);
+    free(sx);
+    free(hq);
+    free(sh);
+    free(y);
+    free(acc);
+}
