@@ -168,6 +168,66 @@ moe_status moe_pack_weights(const float* w13_f32, const float* w2_f32, int H, in
  */
 moe_status moe_quantize_rows(const float* in, int rows, int cols, int ld_in, uint8_t* q, float* s, void* stream);
 
+/*
+ * MXFP8 variant.  "Hosting Qwen on Blackwell" (section "Quantization"): on
+ * Blackwell, FP8 reaches full tensor-core throughput with microscaling, one
+ * power-of-two scale per 32 consecutive values.  The layer above with every
+ * 128x128 / 1x128 quantiser replaced by the OCP MX v1.0 (section 6.3) one:
+ *   for a group of 32 values with absolute maximum amax
+ *     X    = floor(log2(amax)) - 8, clamped to [-127, 127]; scale byte X + 127 (UE8M0)
+ *     code = e4m3_rne_satfinite(v * 2^-X)    (an all-zero group: byte 0, +0 codes)
+ *   x and h in groups of 32 along the row (H, I), weights along K per output row;
+ *   acc = bias + sum_g 2^(sa_g - 127) * 2^(sw_g - 127) * (xq . w)_g, fp32 accumulation.
+ * Same padding (Hp, Ip) and the same blocked code layout as the 128x128
+ * variant.  Scales are bytes in 512-byte ATOMS: one atom per 128x128 code
+ * block, holding that block's 128 rows x 4 groups, byte (r % 32) * 16 +
+ * (r / 32) * 4 + g for row r and group g (the layout the tensor core reads
+ * after tcgen05.cp 32x128b.warpx4):
+ *   s13 uint8 [E, 2*Ip/128, Hp/128, 512]     s2 uint8 [E, Hp/128, Ip/128, 512]
+ * Padding rows and columns get byte 0 and code 0.
+ */
+
+/* Workspace of moe_forward_mx (the same fields as moe_workspace_layout, except
+ * that sx and sh hold scale atoms: [m-tiles, Hp/128, 512] and [m-tiles,
+ * Ip/128, 512], where the rows of expert e form m-tiles of bm rows from
+ * offset[e] -- bm = 32 when T*top_k <= 64*E, else 128 -- and expert e's
+ * m-tiles are numbered from tiles1[e] / (Ip/128)). */
+size_t moe_workspace_size_mx(int T, int H, int I, int E, int top_k);
+moe_status moe_get_workspace_layout_mx(int T, int H, int I, int E, int top_k, moe_workspace_layout* layout);
+
+/*
+ * The MXFP8 layer forward.  Arguments as moe_forward, except s13 and s2: the
+ * scale atoms above (device, 16-byte aligned).  The workspace is sized by
+ * moe_workspace_size_mx.
+ */
+moe_status moe_forward_mx(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
+                          const uint8_t* s13, const void* b13, const uint8_t* w2, const uint8_t* s2, const void* b2,
+                          int T, int H, int I, int E, int top_k, void* out, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* moe_forward_mx with the timing marks of moe_forward_profiled. */
+moe_status moe_forward_mx_profiled(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
+                                   const uint8_t* s13, const void* b13, const uint8_t* w2, const uint8_t* s2,
+                                   const void* b2, int T, int H, int I, int E, int top_k, void* out, void* workspace,
+                                   size_t workspace_bytes, void* stream, void* const* events);
+
+/*
+ * MXFP8 weight packer: fp32 masters (as moe_pack_weights) -> blocked e4m3
+ * codes and scale atoms.  Every output row is quantised along K in groups of
+ * 32.  All output pointers 16-byte aligned; either input may be NULL.
+ */
+moe_status moe_pack_weights_mx(const float* w13_f32, const float* w2_f32, int H, int I, int E, uint8_t* w13,
+                               uint8_t* s13, uint8_t* w2, uint8_t* s2, void* stream);
+
+/*
+ * The 1x32 MX quantiser on its own: in fp32 [rows, cols], row stride ld_in
+ * -> q e4m3 [rows, cp], s uint8 [rows, cp/32] row-major, cp = cols padded to
+ * a multiple of 128 (padding groups: byte 0, codes 0).  Same device
+ * arithmetic as the MX kernels' quantisers.
+ */
+moe_status moe_quantize_rows_mx(const float* in, int rows, int cols, int ld_in, uint8_t* q, uint8_t* s,
+                                void* stream);
+
 /* Synchronises `stream`, then reads and clears the device error word of
  * `workspace`: MOE_OK, MOE_ERR_DEVICE_TIMEOUT (a bounded wait ran out), or
  * MOE_ERR_CUDA. */

@@ -17,7 +17,8 @@ from .build import LIB, build
 
 __all__ = ["MoeError", "build", "lib", "workspace_size", "workspace_layout", "workspace_views", "forward",
            "pack_weights", "pack_weights_into", "w13_shape", "w2_shape", "unblock", "quantize_rows",
-           "read_device_status", "test_bounded_wait", "MoeLayer", "pad128"]
+           "read_device_status", "test_bounded_wait", "MoeLayer", "pad128", "pack_weights_mx",
+           "pack_weights_into_mx", "s13_mx_shape", "s2_mx_shape", "unblock_scales_mx", "quantize_rows_mx"]
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "CUDA error",
           5: "device wait timed out"}
@@ -62,6 +63,18 @@ def lib():
         L.moe_pack_weights.restype = i32
         L.moe_quantize_rows.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         L.moe_quantize_rows.restype = i32
+        L.moe_workspace_size_mx.argtypes = [i32] * 5
+        L.moe_workspace_size_mx.restype = sz
+        L.moe_get_workspace_layout_mx.argtypes = [i32] * 5 + [ctypes.POINTER(_Layout)]
+        L.moe_get_workspace_layout_mx.restype = i32
+        L.moe_forward_mx.argtypes = [vp] * 9 + [i32] * 5 + [vp, vp, sz, vp]
+        L.moe_forward_mx.restype = i32
+        L.moe_forward_mx_profiled.argtypes = [vp] * 9 + [i32] * 5 + [vp, vp, sz, vp, vp]
+        L.moe_forward_mx_profiled.restype = i32
+        L.moe_pack_weights_mx.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+        L.moe_pack_weights_mx.restype = i32
+        L.moe_quantize_rows_mx.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+        L.moe_quantize_rows_mx.restype = i32
         L.moe_read_device_status.argtypes = [vp, vp]
         L.moe_read_device_status.restype = i32
         L.moe_test_bounded_wait.argtypes = [u64, i32, vp, vp]
@@ -96,28 +109,38 @@ def _dev(t: torch.Tensor, dtype, name: str):
     return t.data_ptr()
 
 
-def workspace_size(T: int, H: int, I: int, E: int, top_k: int) -> int:
-    return int(lib().moe_workspace_size(T, H, I, E, top_k))
+def workspace_size(T: int, H: int, I: int, E: int, top_k: int, mx: bool = False) -> int:
+    """Workspace bytes of moe_forward (mx=True: moe_forward_mx)."""
+    f = lib().moe_workspace_size_mx if mx else lib().moe_workspace_size
+    return int(f(T, H, I, E, top_k))
 
 
-def workspace_layout(T: int, H: int, I: int, E: int, top_k: int) -> dict:
+def workspace_layout(T: int, H: int, I: int, E: int, top_k: int, mx: bool = False) -> dict:
     L = _Layout()
-    _check(lib().moe_get_workspace_layout(T, H, I, E, top_k, ctypes.byref(L)), "moe_get_workspace_layout")
+    f = lib().moe_get_workspace_layout_mx if mx else lib().moe_get_workspace_layout
+    _check(f(T, H, I, E, top_k, ctypes.byref(L)), "moe_get_workspace_layout")
     return {f: getattr(L, f) for f in _LAYOUT_FIELDS}
 
 
-def new_workspace(T: int, H: int, I: int, E: int, top_k: int, device=None) -> torch.Tensor:
-    n = workspace_size(T, H, I, E, top_k)
+def new_workspace(T: int, H: int, I: int, E: int, top_k: int, device=None, mx: bool = False) -> torch.Tensor:
+    n = workspace_size(T, H, I, E, top_k, mx)
     if n == 0:
         raise MoeError(1, "workspace_size")
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 
-def workspace_views(ws: torch.Tensor, T: int, H: int, I: int, E: int, top_k: int) -> dict:
-    """Typed views of the intermediates a forward call left in `ws`."""
-    L = workspace_layout(T, H, I, E, top_k)
+def m_tile_rows(T: int, E: int, top_k: int) -> int:
+    """Rows per GEMM m-tile: 32 for decode-sized batches (T*top_k <= 64*E), else 128."""
+    return 32 if T * top_k <= 64 * E else 128
+
+
+def workspace_views(ws: torch.Tensor, T: int, H: int, I: int, E: int, top_k: int, mx: bool = False) -> dict:
+    """Typed views of the intermediates a forward call left in `ws` (mx: of moe_forward_mx,
+    whose sx / sh are scale atoms [m-tiles bound, K blocks, 512] of uint8)."""
+    L = workspace_layout(T, H, I, E, top_k, mx)
     R, Hp, Ip = T * top_k, pad128(H), pad128(I)
     nch = (T + 255) // 256
+    mtb = E + (R + m_tile_rows(T, E, top_k) - 1) // m_tile_rows(T, E, top_k)
 
     def v(name, n, dtype, shape):
         nbytes = n * torch.empty((), dtype=dtype).element_size()
@@ -137,9 +160,11 @@ def workspace_views(ws: torch.Tensor, T: int, H: int, I: int, E: int, top_k: int
         perm=v("perm", R, torch.int32, (R,)),
         inv=v("inv", R, torch.int32, (R,)),
         xq=v("xq", R * Hp, torch.uint8, (R, Hp)),
-        sx=v("sx", R * Hp // 128, torch.float32, (Hp // 128, R)).t(),  # stored K-block-major
+        sx=(v("sx", mtb * Hp // 128 * 512, torch.uint8, (mtb, Hp // 128, 512)) if mx else
+            v("sx", R * Hp // 128, torch.float32, (Hp // 128, R)).t()),  # stored K-block-major
         hq=v("hq", R * Ip, torch.uint8, (R, Ip)),
-        sh=v("sh", R * Ip // 128, torch.float32, (Ip // 128, R)).t(),
+        sh=(v("sh", mtb * Ip // 128 * 512, torch.uint8, (mtb, Ip // 128, 512)) if mx else
+            v("sh", R * Ip // 128, torch.float32, (Ip // 128, R)).t()),
         part=v("part", R * Hp, torch.float32, (R, Hp)),
     )
 
@@ -149,36 +174,45 @@ STAGES = ("router", "permute_quant", "gemm_gateup", "gemm_down", "combine")
 
 def forward(x, router_w, router_b, w13, s13, b13, w2, s2, b2, top_k: int, out=None, workspace=None, stream=None,
             events=None):
-    """out [T, H] bf16 = the MoE layer applied to x [T, H] bf16 (see moe_forward).
+    """out [T, H] bf16 = the MoE layer applied to x [T, H] bf16.
 
-    events: optional list of 6 torch.cuda.Event(enable_timing=True); event i is
-    recorded before stage i (STAGES) and event 5 after the last stage."""
+    Weights from pack_weights (fp32 128x128 block scales: moe_forward) or from
+    pack_weights_mx (uint8 MX scale atoms: moe_forward_mx); the scales' dtype
+    selects the variant.  events: optional list of 6
+    torch.cuda.Event(enable_timing=True); event i is recorded before stage i
+    (STAGES) and event 5 after the last stage."""
     T, H = x.shape
     E = router_w.shape[0]
     I = b13.shape[1] // 2
     Hp, Ip = pad128(H), pad128(I)
+    mx = s13.dtype == torch.uint8
     if tuple(w13.shape) != w13_shape(E, H, I) or tuple(w2.shape) != w2_shape(E, H, I):
         raise ValueError(f"packed weight shapes {tuple(w13.shape)}, {tuple(w2.shape)} do not match H={H} I={I} E={E}")
-    if tuple(s13.shape) != (E, 2 * Ip // 128, Hp // 128) or tuple(s2.shape) != (E, Hp // 128, Ip // 128):
+    if mx:
+        if tuple(s13.shape) != s13_mx_shape(E, H, I) or tuple(s2.shape) != s2_mx_shape(E, H, I):
+            raise ValueError("MX scale atom shapes do not match")
+    elif tuple(s13.shape) != (E, 2 * Ip // 128, Hp // 128) or tuple(s2.shape) != (E, Hp // 128, Ip // 128):
         raise ValueError("block scale shapes do not match")
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
     if workspace is None:
-        workspace = new_workspace(T, H, I, E, top_k, x.device)
+        workspace = new_workspace(T, H, I, E, top_k, x.device, mx)
+    sdt = torch.uint8 if mx else torch.float32
     ptrs = [_dev(x, torch.bfloat16, "x"), _dev(router_w, torch.bfloat16, "router_w"),
-            _dev(router_b, torch.bfloat16, "router_b"), _dev(w13, torch.uint8, "w13"), _dev(s13, torch.float32, "s13"),
-            _dev(b13, torch.bfloat16, "b13"), _dev(w2, torch.uint8, "w2"), _dev(s2, torch.float32, "s2"),
+            _dev(router_b, torch.bfloat16, "router_b"), _dev(w13, torch.uint8, "w13"), _dev(s13, sdt, "s13"),
+            _dev(b13, torch.bfloat16, "b13"), _dev(w2, torch.uint8, "w2"), _dev(s2, sdt, "s2"),
             _dev(b2, torch.bfloat16, "b2")]
     tail = (_dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
             _stream(stream))
+    L = lib()
     if events is None:
-        code = lib().moe_forward(*ptrs, T, H, I, E, top_k, *tail)
+        code = (L.moe_forward_mx if mx else L.moe_forward)(*ptrs, T, H, I, E, top_k, *tail)
     else:
         if len(events) != 6:
             raise ValueError("events must hold 6 CUDA events")
         arr = (ctypes.c_void_p * 6)(*[ev.cuda_event for ev in events])
-        code = lib().moe_forward_profiled(*ptrs, T, H, I, E, top_k, *tail, arr)
-    _check(code, "moe_forward")
+        code = (L.moe_forward_mx_profiled if mx else L.moe_forward_profiled)(*ptrs, T, H, I, E, top_k, *tail, arr)
+    _check(code, "moe_forward_mx" if mx else "moe_forward")
     return out
 
 
@@ -229,6 +263,61 @@ def pack_weights_into(w13_f32, w2_f32, H: int, I: int, E: int, q13, s13, q2, s2,
     _check(code, "moe_pack_weights")
 
 
+def s13_mx_shape(E: int, H: int, I: int) -> tuple:
+    """MX gate/up scale atoms: [E, 2*Ip/128, Hp/128, 512] uint8 (one atom per code block)."""
+    return (E, 2 * pad128(I) // 128, pad128(H) // 128, 512)
+
+
+def s2_mx_shape(E: int, H: int, I: int) -> tuple:
+    """MX down scale atoms: [E, Hp/128, Ip/128, 512] uint8."""
+    return (E, pad128(H) // 128, pad128(I) // 128, 512)
+
+
+def unblock_scales_mx(s: torch.Tensor) -> torch.Tensor:
+    """Scale atoms [E, RB, KB, 512] -> row-major UE8M0 bytes [E, RB*128, KB*4] (for inspection).
+    Atom byte (r % 32) * 16 + (r // 32) * 4 + g holds row r, group g."""
+    E, RB, KB = s.shape[:3]
+    rows = s.reshape(E, RB, KB, 32, 4, 4).permute(0, 1, 2, 4, 3, 5).reshape(E, RB, KB, 128, 4)
+    return rows.permute(0, 1, 3, 2, 4).reshape(E, RB * 128, KB * 4)
+
+
+def pack_weights_mx(w13_f32: torch.Tensor, w2_f32: torch.Tensor, stream=None):
+    """fp32 masters w13 [E, 2I, H], w2 [E, H, I] -> (w13 codes, s13 atoms, w2 codes, s2 atoms), MXFP8."""
+    E, twoI, H = w13_f32.shape
+    I = twoI // 2
+    dev = w13_f32.device
+    if tuple(w2_f32.shape) != (E, H, I):
+        raise ValueError("w2 shape does not match w13")
+    out = (torch.empty(w13_shape(E, H, I), dtype=torch.uint8, device=dev),
+           torch.empty(s13_mx_shape(E, H, I), dtype=torch.uint8, device=dev),
+           torch.empty(w2_shape(E, H, I), dtype=torch.uint8, device=dev),
+           torch.empty(s2_mx_shape(E, H, I), dtype=torch.uint8, device=dev))
+    pack_weights_into_mx(w13_f32, w2_f32, H, I, E, *out, stream=stream)
+    return out
+
+
+def pack_weights_into_mx(w13_f32, w2_f32, H: int, I: int, E: int, q13, s13, q2, s2, stream=None):
+    """MXFP8-pack a slice of experts (either master may be None) into preallocated outputs."""
+    code = lib().moe_pack_weights_mx(None if w13_f32 is None else _dev(w13_f32, torch.float32, "w13_f32"),
+                                     None if w2_f32 is None else _dev(w2_f32, torch.float32, "w2_f32"), H, I, E,
+                                     None if q13 is None else _dev(q13, torch.uint8, "w13"),
+                                     None if s13 is None else _dev(s13, torch.uint8, "s13"),
+                                     None if q2 is None else _dev(q2, torch.uint8, "w2"),
+                                     None if s2 is None else _dev(s2, torch.uint8, "s2"), _stream(stream))
+    _check(code, "moe_pack_weights_mx")
+
+
+def quantize_rows_mx(v: torch.Tensor, stream=None):
+    """1x32 MX quantisation of fp32 rows [rows, cols] -> (codes [rows, cols_p] u8, UE8M0 bytes [rows, cols_p/32])."""
+    rows, cols = v.shape
+    cp = pad128(cols)
+    q = torch.empty((rows, cp), dtype=torch.uint8, device=v.device)
+    s = torch.empty((rows, cp // 32), dtype=torch.uint8, device=v.device)
+    _check(lib().moe_quantize_rows_mx(_dev(v, torch.float32, "v"), rows, cols, cols, q.data_ptr(), s.data_ptr(),
+                                      _stream(stream)), "moe_quantize_rows_mx")
+    return q, s
+
+
 def quantize_rows(v: torch.Tensor, stream=None):
     """1x128 group quantisation of fp32 rows [rows, cols] -> (codes [rows, cols_p] u8, scales [rows, cols_p/128])."""
     rows, cols = v.shape
@@ -263,13 +352,13 @@ class MoeLayer:
         self.top_k = top_k
         self.E, self.H = router_w.shape
         self.I = b13.shape[1] // 2
+        self.mx = s13.dtype == torch.uint8  # MXFP8 scale atoms (pack_weights_mx)
         self._ws = None
-        self._ws_T = -1
 
     def workspace(self, T: int) -> torch.Tensor:
-        if self._ws is None or self._ws_T < T:
-            self._ws = new_workspace(T, self.H, self.I, self.E, self.top_k, self.router_w.device)
-            self._ws_T = T
+        need = workspace_size(T, self.H, self.I, self.E, self.top_k, self.mx)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = new_workspace(T, self.H, self.I, self.E, self.top_k, self.router_w.device, self.mx)
         return self._ws
 
     def __call__(self, x: torch.Tensor, out=None, stream=None) -> torch.Tensor:

@@ -10,7 +10,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
-SOURCES = ["moe_api.cu", "moe_route.cu", "moe_gemm.cu", "moe_gemm_decode.cu"]
+SOURCES = ["moe_api.cu", "moe_route.cu", "moe_gemm.cu", "moe_gemm_decode.cu", "moe_gemm_mx.cu"]
 HEADERS = ["moe_device.cuh", "moe_internal.h"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xptxas", "-v"]

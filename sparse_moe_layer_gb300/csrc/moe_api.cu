@@ -29,7 +29,11 @@ bool sizes_ok(int T, int H, int I, int E, int k) {
     return true;
 }
 
-void layout_of(int T, int H, int I, int E, int k, moe_workspace_layout* L) {
+// Decode-sized batches (few rows per expert) take the weight-streaming
+// kernels with 32-row token tiles; larger ones the 128-row tile kernels.
+inline bool decode_sized(long long R, int E) { return R <= 64LL * E; }
+
+void layout_of(int T, int H, int I, int E, int k, moe_workspace_layout* L, bool mx = false) {
     const size_t R = (size_t)T * k;
     const size_t Hp = pad128(H), Ip = pad128(I);
     const size_t nch = (T + kChunkTokens - 1) / kChunkTokens;
@@ -51,10 +55,13 @@ void layout_of(int T, int H, int I, int E, int k, moe_workspace_layout* L) {
     L->topk_wb = take(R * 2);
     L->perm = take(R * 4);
     L->inv = take(R * 4);
+    // MXFP8: scale atoms per (m-tile, K block); sum_e ceil(count_e/bm) <= E + ceil(R/bm) m-tiles
+    const size_t bm = decode_sized((long long)R, E) ? 32 : 128;
+    const size_t mt_bound = (size_t)E + (R + bm - 1) / bm;
     L->xq = take(R * Hp);
-    L->sx = take(R * (Hp / 128) * 4);
+    L->sx = take(mx ? mt_bound * (Hp / 128) * kMxAtomBytes : R * (Hp / 128) * 4);
     L->hq = take(R * Ip);
-    L->sh = take(R * (Ip / 128) * 4);
+    L->sh = take(mx ? mt_bound * (Ip / 128) * kMxAtomBytes : R * (Ip / 128) * 4);
     L->part = take(R * Hp * 4);
     L->total_bytes = o;
 }
@@ -102,10 +109,11 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Launch sequence shared by moe_forward and moe_forward_profiled; when `ev`
 // is non-null, ev[i] is recorded on the stream before stage i and ev[5]
 // after the last stage.
+// mx: the MXFP8 variant (s13, s2 are UE8M0 scale atoms, not fp32 block scales).
 static moe_status forward_impl(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
-                               const float* s13, const void* b13, const uint8_t* w2, const float* s2, const void* b2,
+                               const void* s13, const void* b13, const uint8_t* w2, const void* s2, const void* b2,
                                int T, int H, int I, int E, int top_k, void* out, void* workspace,
-                               size_t workspace_bytes, void* stream, void* const* ev);
+                               size_t workspace_bytes, void* stream, void* const* ev, bool mx = false);
 
 extern "C" {
 
@@ -140,12 +148,44 @@ moe_status moe_forward_profiled(const void* x, const void* router_w, const void*
                         workspace_bytes, stream, events);
 }
 
+size_t moe_workspace_size_mx(int T, int H, int I, int E, int top_k) {
+    if (!sizes_ok(T, H, I, E, top_k)) return 0;
+    moe_workspace_layout L;
+    layout_of(T, H, I, E, top_k, &L, true);
+    return L.total_bytes;
+}
+
+moe_status moe_get_workspace_layout_mx(int T, int H, int I, int E, int top_k, moe_workspace_layout* layout) {
+    if (!layout || !sizes_ok(T, H, I, E, top_k)) return MOE_ERR_INVALID_ARG;
+    layout_of(T, H, I, E, top_k, layout, true);
+    return MOE_OK;
+}
+
+moe_status moe_forward_mx(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
+                          const uint8_t* s13, const void* b13, const uint8_t* w2, const uint8_t* s2, const void* b2,
+                          int T, int H, int I, int E, int top_k, void* out, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+    return forward_impl(x, router_w, router_b, w13, s13, b13, w2, s2, b2, T, H, I, E, top_k, out, workspace,
+                        workspace_bytes, stream, nullptr, true);
+}
+
+moe_status moe_forward_mx_profiled(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
+                                   const uint8_t* s13, const void* b13, const uint8_t* w2, const uint8_t* s2,
+                                   const void* b2, int T, int H, int I, int E, int top_k, void* out, void* workspace,
+                                   size_t workspace_bytes, void* stream, void* const* events) {
+    if (!events) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 6; ++i)
+        if (!events[i]) return MOE_ERR_INVALID_ARG;
+    return forward_impl(x, router_w, router_b, w13, s13, b13, w2, s2, b2, T, H, I, E, top_k, out, workspace,
+                        workspace_bytes, stream, events, true);
+}
+
 }  // extern "C"
 
 static moe_status forward_impl(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
-                               const float* s13, const void* b13, const uint8_t* w2, const float* s2, const void* b2,
+                               const void* s13, const void* b13, const uint8_t* w2, const void* s2, const void* b2,
                                int T, int H, int I, int E, int top_k, void* out, void* workspace,
-                               size_t workspace_bytes, void* stream, void* const* ev) {
+                               size_t workspace_bytes, void* stream, void* const* ev, bool mx) {
     auto mark = [&](int i) {
         if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), static_cast<cudaStream_t>(stream));
     };
@@ -155,8 +195,9 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     if (!aligned16(x) || !aligned16(router_w) || !aligned16(w13) || !aligned16(w2) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return MOE_ERR_UNSUPPORTED;
+    if (mx && (!aligned16(s13) || !aligned16(s2))) return MOE_ERR_UNSUPPORTED;  // scale atoms move by bulk copy
     moe_workspace_layout L;
-    layout_of(T, H, I, E, top_k, &L);
+    layout_of(T, H, I, E, top_k, &L, mx);
     if (workspace_bytes < L.total_bytes) return MOE_ERR_WORKSPACE;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -182,7 +223,7 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     // Few rows per expert (decode): weight-streaming kernels with 32-row token
     // tiles and 128-feature n-tiles; else 128-row tiles of 128 h features
     // (gate/up) or 256 output features (down: two w2 blocks per tile).
-    const bool decode = (long long)R <= 64LL * E;
+    const bool decode = decode_sized(R, E);
     rp.bm = decode ? 32 : 128;
     rp.nt1 = Ip / 128;
     rp.nt2 = decode ? Hp / 128 : (Hp / 128 + 1) / 2;
@@ -228,6 +269,8 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     pp.xq = ws + L.xq;
     pp.R = R;
     pp.sx = reinterpret_cast<float*>(ws + L.sx);
+    pp.mx = mx ? 1 : 0;
+    pp.sxa = ws + L.sx;
     if (launch_permute_quant(pp, st) != cudaSuccess) return MOE_ERR_CUDA;
     mark(2);
 
@@ -242,6 +285,59 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
         !make_map(&tmA2, ws + L.hq, R, Ip, a_box) || !make_map(&tmB2, w2, (uint64_t)E * Hp * (Ip / 128), 128))
         return MOE_ERR_CUDA;
 
+    if (mx) {
+        MxGemmParams m1;
+        memset(&m1, 0, sizeof(m1));
+        m1.E = E;
+        m1.R = R;
+        m1.KB = Hp / 128;
+        m1.N_real = I;
+        m1.sw_rowblocks = 2 * Ip / 128;
+        m1.up_rows = Ip;
+        m1.nt = rp.nt1;
+        m1.count = rp.count;
+        m1.offset = rp.offset;
+        m1.tiles = rp.tiles1;
+        m1.sa = ws + L.sx;
+        m1.sw = static_cast<const uint8_t*>(s13);
+        m1.bias = static_cast<const uint16_t*>(b13);
+        m1.hq = ws + L.hq;
+        m1.sh = ws + L.sh;
+        m1.ldq = Ip;
+        m1.status = rp.status;
+        const long long t1 = mt_bound * rp.nt1;
+        if (launch_gemm_mx(true, decode, tmA1, tmB1, m1, (int)(t1 < sms ? t1 : sms), st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        mark(3);
+        MxGemmParams m2;
+        memset(&m2, 0, sizeof(m2));
+        m2.E = E;
+        m2.R = R;
+        m2.KB = Ip / 128;
+        m2.N_real = H;
+        m2.sw_rowblocks = Hp / 128;
+        m2.nt = rp.nt2;
+        m2.count = rp.count;
+        m2.offset = rp.offset;
+        m2.tiles = rp.tiles2;
+        m2.sa = ws + L.sh;
+        m2.sw = static_cast<const uint8_t*>(s2);
+        m2.bias = static_cast<const uint16_t*>(b2);
+        m2.perm = pp.perm;
+        m2.topk_wb = rp.topk_wb;
+        m2.part = reinterpret_cast<float*>(ws + L.part);
+        m2.ldp = Hp;
+        m2.status = rp.status;
+        const long long t2 = mt_bound * rp.nt2;
+        if (launch_gemm_mx(false, decode, tmA2, tmB2, m2, (int)(t2 < sms ? t2 : sms), st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        mark(4);
+        if (launch_combine(m2.part, T, H, Hp, top_k, static_cast<uint16_t*>(out), sms, st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        mark(5);
+        return MOE_OK;
+    }
+
     GemmParams g1;
     memset(&g1, 0, sizeof(g1));
     g1.E = E;
@@ -255,7 +351,7 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     g1.offset = rp.offset;
     g1.tiles = rp.tiles1;
     g1.sa = pp.sx;
-    g1.sw = s13;
+    g1.sw = static_cast<const float*>(s13);
     g1.bias = static_cast<const uint16_t*>(b13);
     g1.hq = ws + L.hq;
     g1.sh = reinterpret_cast<float*>(ws + L.sh);
@@ -281,7 +377,7 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     g2.offset = rp.offset;
     g2.tiles = rp.tiles2;
     g2.sa = g1.sh;
-    g2.sw = s2;
+    g2.sw = static_cast<const float*>(s2);
     g2.bias = static_cast<const uint16_t*>(b2);
     g2.perm = pp.perm;
     g2.topk_wb = rp.topk_wb;
@@ -362,6 +458,30 @@ moe_status moe_pack_weights(const float* w13_f32, const float* w2_f32, int H, in
     if (w13_f32 && launch_pack_blocks(w13_f32, E, 2 * I, H, 2 * Ip, Hp, I, w13, s13, st) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (w2_f32 && launch_pack_blocks(w2_f32, E, H, I, Hp, Ip, 0, w2, s2, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status moe_pack_weights_mx(const float* w13_f32, const float* w2_f32, int H, int I, int E, uint8_t* w13,
+                               uint8_t* s13, uint8_t* w2, uint8_t* s2, void* stream) {
+    if (H < 1 || I < 1 || E < 1 || H > 16384 || I > 16384 || E > kMaxExperts) return MOE_ERR_INVALID_ARG;
+    if (!w13_f32 && !w2_f32) return MOE_ERR_INVALID_ARG;
+    if ((w13_f32 && (!w13 || !s13)) || (w2_f32 && (!w2 || !s2))) return MOE_ERR_INVALID_ARG;
+    if ((w13 && !aligned16(w13)) || (w2 && !aligned16(w2)) || (s13 && !aligned16(s13)) || (s2 && !aligned16(s2)))
+        return MOE_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int Hp = pad128(H), Ip = pad128(I);
+    if (w13_f32 && launch_pack_blocks_mx(w13_f32, E, 2 * I, H, 2 * Ip, Hp, I, w13, s13, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (w2_f32 && launch_pack_blocks_mx(w2_f32, E, H, I, Hp, Ip, 0, w2, s2, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status moe_quantize_rows_mx(const float* in, int rows, int cols, int ld_in, uint8_t* q, uint8_t* s,
+                                void* stream) {
+    if (!in || !q || !s || rows < 1 || cols < 1 || ld_in < cols) return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(q) & 3u) return MOE_ERR_UNSUPPORTED;
+    if (launch_quantize_rows_mx(in, rows, cols, ld_in, q, s, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
     return MOE_OK;
 }
 

@@ -70,6 +70,46 @@ __device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, f
     return e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s)) | (e4m3x2(__fdiv_rn(c, s), __fdiv_rn(d, s)) << 16);
 }
 
+// ----------------------------------------------------- MXFP8 quantiser ----
+// OCP Microscaling Formats (MX) v1.0, section 6.3, for a group of 32 values
+// with absolute maximum amax: shared exponent X = floor(log2(amax)) - 8 (8 =
+// the exponent of e4m3's largest normal), stored as the UE8M0 byte X + 127;
+// codes e4m3_rne_satfinite(v * 2^-X).  X is clamped to [-127, 127] and an
+// all-zero group gets the byte 0 and +0 codes.  For amax > 0 with biased
+// fp32 exponent b (0 for a subnormal amax), floor(log2(amax)) = b - 127 for
+// a normal amax, and every amax below 2^-119 lands on the clamp, so the
+// byte is max(b - 8, 0); a finite amax never reaches the upper clamp.
+__device__ __forceinline__ uint32_t mx_scale_byte(float amax) {
+    const int b = (int)((__float_as_uint(amax) >> 23) & 0xffu);
+    return amax == 0.0f ? 0u : (uint32_t)max(b - 8, 0);
+}
+// 2^-X = 2^(127 - byte) as an fp32 (a normal number for every byte in [0, 246]).
+__device__ __forceinline__ float mx_inv_scale(uint32_t byte) { return __uint_as_float((254u - byte) << 23); }
+// Sign mask of a group's scaled values: an all-zero group's codes are +0.
+__device__ __forceinline__ uint32_t mx_keep(float amax) { return amax == 0.0f ? 0x7fffffffu : 0xffffffffu; }
+// v * 2^-X rounded once to fp32 (exact unless it underflows, and then far
+// below the smallest e4m3 subnormal), sign-masked.
+__device__ __forceinline__ float mx_scaled(float v, float inv, uint32_t keep) {
+    return __uint_as_float(__float_as_uint(__fmul_rn(v, inv)) & keep);
+}
+__device__ __forceinline__ uint32_t mx_quant4(float a, float b, float c, float d, float inv, uint32_t keep) {
+    return e4m3x2(mx_scaled(a, inv, keep), mx_scaled(b, inv, keep)) |
+           (e4m3x2(mx_scaled(c, inv, keep), mx_scaled(d, inv, keep)) << 16);
+}
+
+// Scale atoms.  The block-scaled MMA (kind::mxf8f6f4, scale_vec::1X) reads
+// the scale of A row m from TMEM lane m, column sfa + m/32, and the scale of
+// B column n from the lane (n mod 32) of the accumulator row's lane quarter,
+// column sfb + n/32; the byte of the 32-bit cell is the MMA's scale id, here
+// the 32-wide K group inside a 128-wide K block.  tcgen05.cp 32x128b.warpx4
+// copies 32 rows of 16 bytes into 4 columns of lanes 0-31 and replicates
+// them into the other three quarters, so one 512-byte atom serves 128 rows
+// (or columns) x one K block: byte (r % 32) * 16 + (r / 32) * 4 + g for row
+// r and K group g.  Weight blocks, activation tiles and token tiles all use
+// this atom.
+__host__ __device__ constexpr int mx_atom_byte(int r, int g) { return (r & 31) * 16 + (r >> 5) * 4 + g; }
+constexpr int kMxAtomBytes = 512;
+
 // 2^x and 1/x from the special-function unit (PTX ex2.approx / rcp.approx,
 // subnormals flushed): one instruction each, no branches.
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -231,6 +271,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
+// Contiguous copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from global to shared memory, completing on mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // -------------------------------------------------------------- tcgen05 ----
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
@@ -273,6 +321,41 @@ __device__ __forceinline__ void mma_e4m3(uint32_t tmem_d, uint64_t adesc, uint64
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// Block-scaled MMA (kind::mxf8f6f4, one UE8M0 scale per 32 K values of each
+// A row and each B column): instruction descriptor without the scale ids
+// (A = B = e4m3, fp32 D, both K-major, bit 23 = UE8M0 scales) ...
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N) {
+    return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+// ... with the byte of the scale cells this MMA reads (B: bits 4-5, A: bits 29-30).
+__device__ __forceinline__ uint32_t idesc_sf_id(uint32_t idesc, uint32_t id) { return idesc | (id << 4) | (id << 29); }
+
+__device__ __forceinline__ void mma_mx(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+// Shared-memory descriptor of one 512-byte scale atom (32 rows of 16 bytes,
+// no swizzle: 8-row groups 128 bytes apart) ...
+__device__ __forceinline__ uint64_t smem_desc_atom(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFF);
+    d |= (uint64_t)(128 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+// ... copied into TMEM columns [taddr, taddr + 4) of every lane quarter.
+// Ordered before the MMAs this thread issues after it.
+__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint32_t smem_addr) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(smem_desc_atom(smem_addr))
+                 : "memory");
 }
 
 // Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.

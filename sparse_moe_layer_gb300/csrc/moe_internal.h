@@ -50,6 +50,10 @@ struct PermuteParams {
     int R;        // T * k
     uint8_t* xq;  // [R, Hp]
     float* sx;    // [Hp/128, R] (K-block-major)
+    // MXFP8 variant: 1x32 UE8M0 scales into scale atoms [m-tiles, Hp/128, 512]
+    // (m-tile of row r of expert e: tiles1[e]/nt1 + (r - offset[e])/bm)
+    int mx;
+    uint8_t* sxa;
 };
 
 constexpr int kDecXBoxRows = 8;  // activation rows per TMA box of the decode GEMMs
@@ -76,6 +80,31 @@ struct GemmParams {
     const uint16_t* bias;  // gate/up: b13 [E, 2I]; down: b2 [E, H]
     uint8_t* hq;           // gate/up output codes [R, ldq]
     float* sh;             // gate/up output scales [ldq/128, R] (K-block-major)
+    int ldq;
+    const int32_t* perm;      // down: row -> t*k + j
+    const uint16_t* topk_wb;  // down: routing weights bf16 [T*k]
+    float* part;              // down: [T*k, ldp]
+    int ldp;
+    uint32_t* status;
+};
+
+// The MXFP8 GEMMs: scales are UE8M0 bytes in 512-byte atoms (one per 128
+// rows x one 128-wide K block, mx_atom_byte layout); the tile list is the same
+// as the 128x128 variant's.
+struct MxGemmParams {
+    int E, R, KB;          // K / 128
+    int N_real;            // gate/up GEMM: I; down GEMM: H
+    int sw_rowblocks;      // rows of one expert's weight matrix / 128
+    int up_rows;           // gate/up GEMM: Ip (row offset of the up half)
+    int nt;                // n-tiles per m-tile (tiles[e] = nt * m-tiles of the experts before e)
+    const int32_t* count;
+    const int32_t* offset;
+    const int32_t* tiles;  // [E+1] first tile of each expert
+    const uint8_t* sa;     // activation scale atoms [m-tiles, KB, 512]
+    const uint8_t* sw;     // weight scale atoms [E, sw_rowblocks, KB, 512]
+    const uint16_t* bias;  // gate/up: b13 [E, 2I]; down: b2 [E, H]
+    uint8_t* hq;           // gate/up output codes [R, ldq]
+    uint8_t* sh;           // gate/up output scale atoms [m-tiles, ldq/128, 512]
     int ldq;
     const int32_t* perm;      // down: row -> t*k + j
     const uint16_t* topk_wb;  // down: routing weights bf16 [T*k]
@@ -111,6 +140,10 @@ cudaError_t launch_pack_blocks(const float* src, int E, int rows_src, int cols, 
                                uint8_t* q, float* s, cudaStream_t st);
 cudaError_t launch_quantize_rows(const float* in, int rows, int cols, int ld_in, uint8_t* q, float* s,
                                  cudaStream_t st);
+cudaError_t launch_pack_blocks_mx(const float* src, int E, int rows_src, int cols, int rows_p, int cols_p, int gated_I,
+                                  uint8_t* q, uint8_t* s, cudaStream_t st);
+cudaError_t launch_quantize_rows_mx(const float* in, int rows, int cols, int ld_in, uint8_t* q, uint8_t* s,
+                                    cudaStream_t st);
 cudaError_t launch_bounded_wait_test(uint64_t timeout_ns, int arrivals, uint32_t* result, cudaStream_t st);
 cudaError_t launch_gemm_gateup(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
                                cudaStream_t st);
@@ -120,5 +153,9 @@ cudaError_t launch_gemm_gateup_decode(const CUtensorMap& tmW, const CUtensorMap&
                                       cudaStream_t st);
 cudaError_t launch_gemm_down_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int grid,
                                     cudaStream_t st);
+
+// tmX: activation rows (prefill: 128-row boxes, decode: kDecXBoxRows-row boxes); tmW: blocked weights
+cudaError_t launch_gemm_mx(bool gated, bool decode, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                           const MxGemmParams& p, int grid, cudaStream_t st);
 
 }  // namespace moe

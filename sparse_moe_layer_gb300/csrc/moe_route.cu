@@ -351,6 +351,8 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
     __shared__ int s_base[kMaxExperts];
     __shared__ int s_idx[8 * kMaxTopK];
     __shared__ int s_row[8 * kMaxTopK];
+    __shared__ int s_eoff[kMaxExperts];  // MXFP8: first row of each expert ...
+    __shared__ int s_emt[kMaxExperts];   // ... and the m-tiles of the experts before it
     const int tpc = p.tokens_per_cta;
     const int t0 = blockIdx.x * tpc;
     const int chunk = t0 / kChunkTokens;
@@ -413,6 +415,8 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
                 const int e = lane * 8 + i;
                 if (e < p.E) {
                     s_base[e] += off;
+                    s_eoff[e] = off;
+                    s_emt[e] = mts;
                     if (blockIdx.x == 0) {
                         p.offset[e] = off;
                         p.count[e] = cnt[i];
@@ -435,7 +439,13 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
         __syncthreads();
         for (int e = threadIdx.x; e < p.E; e += blockDim.x) s_pre[e] = 0;
     } else {
-        for (int e = threadIdx.x; e < p.E; e += blockDim.x) s_base[e] = p.chunk_base[(size_t)chunk * p.E + e];
+        for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+            s_base[e] = p.chunk_base[(size_t)chunk * p.E + e];
+            if (p.mx) {
+                s_eoff[e] = p.offset[e];
+                s_emt[e] = p.tiles1[e] / p.nt1;
+            }
+        }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < (t0 - c0) * p.k; i += blockDim.x) atomicAdd(&s_pre[p.topk_idx[(size_t)c0 * p.k + i]], 1);
@@ -470,6 +480,28 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
             for (int i = 0; i < 4; ++i) a[i] = (c + i < Hx) ? bf16_bits_to_f32(xs[tt * Hx + c + i]) : 0.f;
         }
         float amax = fmaxf(fmaxf(fabsf(a[0]), fabsf(a[1])), fmaxf(fabsf(a[2]), fabsf(a[3])));
+        if (p.mx) {
+            // 1x32 groups: lanes 8q..8q+7 hold group q of this 128-wide K block
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const uint32_t sb = mx_scale_byte(amax);
+            const uint32_t q = mx_quant4(a[0], a[1], a[2], a[3], mx_inv_scale(sb), mx_keep(amax));
+            // the block's four scale bytes, one 32-bit cell of the row's atom
+            const uint32_t cell = __shfl_sync(0xffffffffu, sb, 0) | (__shfl_sync(0xffffffffu, sb, 8) << 8) |
+                                  (__shfl_sync(0xffffffffu, sb, 16) << 16) | (__shfl_sync(0xffffffffu, sb, 24) << 24);
+            for (int j = 0; j < p.k; ++j) {
+                const int r = s_row[tt * p.k + j];
+                *reinterpret_cast<uint32_t*>(p.xq + (size_t)r * p.Hp + c) = q;
+                if (lane == 0) {
+                    const int e = s_idx[tt * p.k + j];
+                    const int local = r - s_eoff[e];
+                    const int mt = s_emt[e] + local / p.bm, m = local % p.bm;
+                    *reinterpret_cast<uint32_t*>(p.sxa + ((size_t)mt * G + g) * kMxAtomBytes + mx_atom_byte(m, 0)) =
+                        cell;
+                }
+            }
+            continue;
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         const float s = group_scale(amax);
@@ -626,6 +658,95 @@ cudaError_t launch_quantize_rows(const float* in, int rows, int cols, int ld_in,
     int grid = (int)(blocks < 4096 ? blocks : 4096);
     if (grid < 1) grid = 1;
     quantize_rows_kernel<<<grid, 256, 0, st>>>(in, rows, cols, ld_in, q, s);
+    return cudaGetLastError();
+}
+
+// ======================================================= MXFP8 weight packer
+// Same blocks and row mapping as pack_blocks_kernel; every weight row is
+// quantised along K in groups of 32 (mx_scale_byte / mx_quant4), and the
+// block's 128 rows x 4 groups of scale bytes form one 512-byte atom
+// (mx_atom_byte), stored [E][row block][K block][512] beside the codes.
+__global__ void __launch_bounds__(256) pack_blocks_mx_kernel(const float* __restrict__ src, int rows_src, int cols,
+                                                             int rows_p, int cols_p, int gated_I,
+                                                             uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+    const int bj = blockIdx.x, bi = blockIdx.y, e = blockIdx.z;
+    const int r_local = threadIdx.x >> 1, half = threadIdx.x & 1;
+    const int dr = bi * 128 + r_local;
+    const int c0 = bj * 128 + half * 64;
+    int sr;
+    if (gated_I > 0) {
+        const int Ip = rows_p / 2;
+        sr = dr < Ip ? (dr < gated_I ? dr : -1) : (dr - Ip < gated_I ? gated_I + dr - Ip : -1);
+    } else {
+        sr = dr < rows_src ? dr : -1;
+    }
+    const float* row = sr >= 0 ? src + ((size_t)e * rows_src + sr) * cols : nullptr;
+    const size_t blk = ((size_t)e * (rows_p / 128) + bi) * (cols_p / 128) + bj;
+    uint32_t packed[16];
+    uint32_t bytes = 0;
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        float v[32];
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int c = c0 + 32 * g + i;
+            v[i] = (row && c < cols) ? __ldg(row + c) : 0.f;
+            amax = fmaxf(amax, fabsf(v[i]));
+        }
+        const uint32_t sb = mx_scale_byte(amax);
+        const float inv = mx_inv_scale(sb);
+        const uint32_t keep = mx_keep(amax);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) packed[8 * g + i] = mx_quant4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], inv, keep);
+        bytes |= sb << (8 * g);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(q + blk * 16384 + (size_t)r_local * 128 + half * 64);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+    *reinterpret_cast<uint16_t*>(s + blk * kMxAtomBytes + mx_atom_byte(r_local, 2 * half)) = (uint16_t)bytes;
+}
+
+cudaError_t launch_pack_blocks_mx(const float* src, int E, int rows_src, int cols, int rows_p, int cols_p, int gated_I,
+                                  uint8_t* q, uint8_t* s, cudaStream_t st) {
+    dim3 grid(cols_p / 128, rows_p / 128, E);
+    pack_blocks_mx_kernel<<<grid, 256, 0, st>>>(src, rows_src, cols, rows_p, cols_p, gated_I, q, s);
+    return cudaGetLastError();
+}
+
+// ============================================== stand-alone 1x32 quantiser
+// fp32 [rows, cols] -> codes [rows, cp], scale bytes [rows, cp/32] (row-major,
+// cp = cols padded to 128); one warp per 128-wide block, 8 lanes per group.
+__global__ void __launch_bounds__(256) quantize_rows_mx_kernel(const float* __restrict__ in, int rows, int cols,
+                                                               int ld_in, uint8_t* __restrict__ q,
+                                                               uint8_t* __restrict__ s) {
+    const int G = (cols + 127) / 128;
+    const int cp = G * 128;
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (long item = warp; item < (long)rows * G; item += nwarps) {
+        const int r = (int)(item / G), g = (int)(item - (long)r * G);
+        const int c = g * 128 + lane * 4;
+        float a[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = (c + i < cols) ? in[(size_t)r * ld_in + c + i] : 0.f;
+        float amax = fmaxf(fmaxf(fabsf(a[0]), fabsf(a[1])), fmaxf(fabsf(a[2]), fabsf(a[3])));
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const uint32_t sb = mx_scale_byte(amax);
+        *reinterpret_cast<uint32_t*>(q + (size_t)r * cp + c) =
+            mx_quant4(a[0], a[1], a[2], a[3], mx_inv_scale(sb), mx_keep(amax));
+        if ((lane & 7) == 0) s[(size_t)r * (cp / 32) + g * 4 + (lane >> 3)] = (uint8_t)sb;
+    }
+}
+
+cudaError_t launch_quantize_rows_mx(const float* in, int rows, int cols, int ld_in, uint8_t* q, uint8_t* s,
+                                    cudaStream_t st) {
+    long items = (long)rows * ((cols + 127) / 128);
+    long blocks = (items + 7) / 8;
+    int grid = (int)(blocks < 4096 ? blocks : 4096);
+    if (grid < 1) grid = 1;
+    quantize_rows_mx_kernel<<<grid, 256, 0, st>>>(in, rows, cols, ld_in, q, s);
     return cudaGetLastError();
 }
 

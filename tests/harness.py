@@ -38,8 +38,9 @@ class Layer:
     """Inputs of one layer shape: host arrays (bf16 as uint16 bits) plus device tensors."""
 
     def __init__(self, cfg: synth.LayerConfig, x: np.ndarray | None = None, rw=None, rb=None, b13=None, b2=None,
-                 w13_master=None, w2_master=None):
+                 w13_master=None, w2_master=None, mx: bool = False):
         self.cfg = cfg
+        self.mx = mx  # MXFP8 variant (1x32 UE8M0 scales) instead of 128x128 / 1x128 fp32 scales
         self.T, self.H, self.I, self.E, self.k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k
         self.Hp, self.Ip = cfg.Hp, cfg.Ip
         self.x = synth.layer_x(cfg) if x is None else x
@@ -74,15 +75,20 @@ class Layer:
         self.d_b13 = bf16_np_to_torch(self.b13)
         self.d_b2 = bf16_np_to_torch(self.b2)
         self.d_w13 = torch.empty(moe.w13_shape(E, H, I), dtype=torch.uint8, device=dev)
-        self.d_s13 = torch.empty((E, 2 * Ip // 128, Hp // 128), dtype=torch.float32, device=dev)
         self.d_w2 = torch.empty(moe.w2_shape(E, H, I), dtype=torch.uint8, device=dev)
-        self.d_s2 = torch.empty((E, Hp // 128, Ip // 128), dtype=torch.float32, device=dev)
+        if self.mx:
+            self.d_s13 = torch.empty(moe.s13_mx_shape(E, H, I), dtype=torch.uint8, device=dev)
+            self.d_s2 = torch.empty(moe.s2_mx_shape(E, H, I), dtype=torch.uint8, device=dev)
+        else:
+            self.d_s13 = torch.empty((E, 2 * Ip // 128, Hp // 128), dtype=torch.float32, device=dev)
+            self.d_s2 = torch.empty((E, Hp // 128, Ip // 128), dtype=torch.float32, device=dev)
+        pack = moe.pack_weights_into_mx if self.mx else moe.pack_weights_into
         for e0 in range(0, E, chunk_experts):
             n = min(chunk_experts, E - e0)
             m13 = torch.from_numpy(self.w13_master(e0, n)).to(dev)
             m2 = torch.from_numpy(self.w2_master(e0, n)).to(dev)
-            moe.pack_weights_into(m13, m2, H, I, n, self.d_w13[e0:e0 + n], self.d_s13[e0:e0 + n],
-                                  self.d_w2[e0:e0 + n], self.d_s2[e0:e0 + n])
+            pack(m13, m2, H, I, n, self.d_w13[e0:e0 + n], self.d_s13[e0:e0 + n], self.d_w2[e0:e0 + n],
+                 self.d_s2[e0:e0 + n])
             torch.cuda.synchronize()
             del m13, m2
         return self
@@ -90,11 +96,11 @@ class Layer:
     def run_gpu(self, workspace=None):
         import sparse_moe_layer_gb300 as moe
         if workspace is None:
-            workspace = moe.new_workspace(self.T, self.H, self.I, self.E, self.k)
+            workspace = moe.new_workspace(self.T, self.H, self.I, self.E, self.k, mx=self.mx)
         out = moe.forward(self.d_x, self.d_rw, self.d_rb, self.d_w13, self.d_s13, self.d_b13, self.d_w2, self.d_s2,
                           self.d_b2, self.k, workspace=workspace)
         torch.cuda.synchronize()
-        views = moe.workspace_views(workspace, self.T, self.H, self.I, self.E, self.k)
+        views = moe.workspace_views(workspace, self.T, self.H, self.I, self.E, self.k, mx=self.mx)
         return out, views, workspace
 
     # ---- oracle side ----
@@ -102,14 +108,19 @@ class Layer:
         """Oracle-packed codes/scales as full [E, ...] arrays with only `experts` filled."""
         E, Hp, Ip = self.E, self.Hp, self.Ip
         if self._oq is None:
-            self._oq = (np.zeros((E, 2 * Ip, Hp), np.uint8), np.ones((E, 2 * Ip // 128, Hp // 128), np.float32),
-                        np.zeros((E, Hp, Ip), np.uint8), np.ones((E, Hp // 128, Ip // 128), np.float32), set())
+            if self.mx:
+                self._oq = (np.zeros((E, 2 * Ip, Hp), np.uint8), np.zeros((E, 2 * Ip, Hp // 32), np.uint8),
+                            np.zeros((E, Hp, Ip), np.uint8), np.zeros((E, Hp, Ip // 32), np.uint8), set())
+            else:
+                self._oq = (np.zeros((E, 2 * Ip, Hp), np.uint8), np.ones((E, 2 * Ip // 128, Hp // 128), np.float32),
+                            np.zeros((E, Hp, Ip), np.uint8), np.ones((E, Hp // 128, Ip // 128), np.float32), set())
         q13, s13, q2, s2, done = self._oq
         todo = sorted(set(int(e) for e in experts) - done)
+        p13, p2 = (oracle.mx_pack_w13, oracle.mx_pack_w2) if self.mx else (oracle.pack_w13, oracle.pack_w2)
 
         def one(e):
-            oracle.pack_w13(self.w13_master(e, 1), q13[e:e + 1], s13[e:e + 1])
-            oracle.pack_w2(self.w2_master(e, 1), q2[e:e + 1], s2[e:e + 1])
+            p13(self.w13_master(e, 1), q13[e:e + 1], s13[e:e + 1])
+            p2(self.w2_master(e, 1), q2[e:e + 1], s2[e:e + 1])
 
         with ThreadPoolExecutor(max_workers=threads()) as ex:
             list(ex.map(one, todo))
@@ -134,15 +145,35 @@ class Layer:
         q13, s13, q2, s2 = self.oracle_weights(np.unique(idx_all[tokens]))
         chunks = [c for c in np.array_split(tokens, max(1, min(len(tokens), threads()))) if len(c)]
 
+        fwd = oracle.mx_forward if self.mx else oracle.forward
+
         def one(c):
-            return oracle.forward(self.x, self.rw, self.rb, q13, s13, self.b13, q2, s2, self.b2, self.k, tokens=c,
-                                  want_intermediates=True)
+            return fwd(self.x, self.rw, self.rb, q13, s13, self.b13, q2, s2, self.b2, self.k, tokens=c,
+                       want_intermediates=True)
 
         with ThreadPoolExecutor(max_workers=threads()) as ex:
             parts = list(ex.map(one, chunks))
         out = np.concatenate([p[0] for p in parts])
         inter = {key: np.concatenate([p[1][key] for p in parts]) for key in parts[0][1]}
         return out, inter
+
+
+def mx_row_scales(atoms: np.ndarray, count: np.ndarray, offset: np.ndarray, tiles: np.ndarray, nt: int,
+                  bm: int) -> np.ndarray:
+    """Activation scale atoms [m-tiles, KB, 512] -> UE8M0 bytes [R, KB*4] by permuted row.
+    Row r of expert e sits in m-tile tiles[e]/nt + (r - offset[e]) // bm at row
+    m = (r - offset[e]) % bm of that tile; the atom byte of (m, group g) is
+    (m % 32) * 16 + (m // 32) * 4 + g."""
+    KB = atoms.shape[1]
+    R = int(offset[-1])
+    out = np.zeros((R, KB * 4), np.uint8)
+    for e in range(len(count)):
+        for r in range(int(offset[e]), int(offset[e]) + int(count[e])):
+            local = r - int(offset[e])
+            mt, m = int(tiles[e]) // nt + local // bm, local % bm
+            byte = (m % 32) * 16 + (m // 32) * 4
+            out[r] = atoms[mt, :, byte:byte + 4].reshape(-1)
+    return out
 
 
 def sample_tokens(idx: np.ndarray, E: int, n: int, seed: int = 0) -> np.ndarray:

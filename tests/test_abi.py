@@ -61,6 +61,37 @@ def test_host_argument_checks(moe):
     assert L.moe_status_str(5) == b"a bounded device-side wait timed out"
 
 
+def test_mx_host_argument_checks_and_layout(moe):
+    L = moe.lib()
+    for f in ("moe_forward_mx", "moe_forward_mx_profiled", "moe_pack_weights_mx", "moe_quantize_rows_mx",
+              "moe_workspace_size_mx", "moe_get_workspace_layout_mx"):
+        assert f in declared_functions()
+    assert L.moe_workspace_size_mx(0, 256, 256, 8, 2) == 0
+    args = [None] * 9 + [64, 256, 256, 8, 2, None, None, 0, None]
+    assert L.moe_forward_mx(*args) == 1
+    assert L.moe_pack_weights_mx(None, None, 256, 256, 8, None, None, None, None, None) == 1
+    assert L.moe_quantize_rows_mx(None, 4, 4, 4, None, None, None) == 1
+    # scale atoms: one 512-byte atom per (m-tile, K block); m-tiles <= E + ceil(R / bm)
+    for T, E, k, bm in ((64, 32, 4, 32), (8192, 128, 4, 128)):
+        R, Hp, Ip = T * k, 2944, 2944
+        lay = moe.workspace_layout(T, 2880, 2880, E, k, mx=True)
+        mtb = E + (R + bm - 1) // bm
+        assert moe.m_tile_rows(T, E, k) == bm
+        assert lay["xq"] + R * Hp <= lay["sx"] and lay["sx"] + mtb * (Hp // 128) * 512 <= lay["hq"]
+        assert lay["hq"] + R * Ip <= lay["sh"] and lay["sh"] + mtb * (Ip // 128) * 512 <= lay["part"]
+        assert all(lay[f] % 256 == 0 for f in ("sx", "sh", "part"))
+        assert moe.workspace_size(T, 2880, 2880, E, k, mx=True) == lay["total_bytes"]
+
+
+def test_mx_scale_atom_unblocking(moe):
+    import torch
+    s = (torch.arange(2 * 3 * 2 * 512) % 251).to(torch.uint8).reshape(2, 3, 2, 512)
+    u = moe.unblock_scales_mx(s)
+    assert tuple(u.shape) == (2, 3 * 128, 2 * 4)
+    for e, rb, kb, r, g in ((0, 0, 0, 0, 0), (1, 2, 1, 77, 3), (0, 1, 0, 127, 2), (1, 0, 1, 33, 1)):
+        assert int(u[e, rb * 128 + r, kb * 4 + g]) == int(s[e, rb, kb, (r % 32) * 16 + (r // 32) * 4 + g])
+
+
 def test_product_sources_do_not_reach_the_oracle():
     pkg = os.path.join(ROOT, "sparse_moe_layer_gb300")
     for dirpath, _, files in os.walk(pkg):
