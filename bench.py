@@ -9,6 +9,11 @@ and the step is timed with CUDA events on the launching stream; the flush is
 outside the events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+                  [--format block128|mx]
+
+--format mx runs the MXFP8 variant (1x32 UE8M0 scales on both operands,
+block-scaled tensor-core MMA) on the same workload; the default is the layer
+with 128x128 weight / 1x128 activation block scales.
 
 Multi-GPU: one process per GPU (torchrun), each an independent replica of the
 same workload (the layer has no exchange step on one GPU): weak scaling,
@@ -34,6 +39,8 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/s on 1 GB300; % of HBM (decode) / FP8 TC peak (prefill)"
+WEIGHTS = {"block128": "FP8 e4m3 128x128 block scales (x, h: 1x128), packed on device by moe_pack_weights",
+           "mx": "MXFP8: e4m3 with 1x32 UE8M0 scales on weights, x and h, packed on device by moe_pack_weights_mx"}
 DEFAULT_CONFIG = "oss20b_decode"
 FLUSH_BYTES = 256 << 20
 
@@ -53,36 +60,47 @@ def workload_str(cfg) -> str:
             f"router_b={cfg.router_b} expert_bias={cfg.expert_bias}")
 
 
-def algorithmic(cfg, counts: np.ndarray) -> dict:
-    """Algorithmic bytes / FLOPs (unpadded; activated experts only)."""
+def algorithmic(cfg, counts: np.ndarray, mx: bool = False) -> dict:
+    """Algorithmic bytes / FLOPs (unpadded; activated experts only).  Scales:
+    fp32 per 128x128 weight block and per 1x128 activation group, or (mx) one
+    byte per 32 values of every weight row and activation row."""
     H, I, T, k, E = cfg.H, cfg.I, cfg.T, cfg.top_k, cfg.E
     R = T * k
     act = int((counts > 0).sum())
     hb, ib = -(-H // 128), -(-I // 128)
-    w13 = act * (2 * I * H + 4 * 2 * ib * hb + 2 * 2 * I)
-    w2 = act * (H * I + 4 * hb * ib + 2 * H)
-    gemm1_bytes = w13 + R * H + 4 * R * hb + R * I + 4 * R * ib
-    gemm2_bytes = w2 + R * I + 4 * R * ib + 4 * R * H
+    if mx:
+        hg, ig = -(-H // 32), -(-I // 32)
+        w13 = act * (2 * I * H + 2 * I * hg + 2 * 2 * I)
+        w2 = act * (H * I + H * ig + 2 * H)
+        sxb, shb = R * hg, R * ig
+    else:
+        w13 = act * (2 * I * H + 4 * 2 * ib * hb + 2 * 2 * I)
+        w2 = act * (H * I + 4 * hb * ib + 2 * H)
+        sxb, shb = 4 * R * hb, 4 * R * ib
+    gemm1_bytes = w13 + R * H + sxb + R * I + shb
+    gemm2_bytes = w2 + R * I + shb + 4 * R * H
     step_bytes = w13 + w2 + E * H * 2 + E * 2 + T * H * 2 + T * H * 2
     return dict(active=act, gemm1_bytes=gemm1_bytes, gemm2_bytes=gemm2_bytes, step_bytes=step_bytes,
                 gemm1_flops=2 * R * 2 * I * H, gemm2_flops=2 * R * H * I, router_flops=2 * T * E * H)
 
 
-def source_digest() -> str:
+def source_digest(mx: bool = False) -> str:
+    """Digest of the GEMM kernels' sources (ncu traffic is valid only for the source it was taken on)."""
     h = hashlib.sha256()
-    for f in ("moe_gemm.cu", "moe_gemm_decode.cu", "moe_device.cuh", "moe_internal.h"):
+    files = ("moe_gemm_mx.cu",) if mx else ("moe_gemm.cu", "moe_gemm_decode.cu")
+    for f in files + ("moe_device.cuh", "moe_internal.h"):
         with open(os.path.join(ROOT, "sparse_moe_layer_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, cfg_name: str):
+def recorded_traffic(kernel: str, cfg_name: str, mx: bool = False):
     """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel source."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             t = json.load(f)
         rec = t.get(f"{kernel}@{cfg_name}")
-        if rec and rec.get("source_digest") == source_digest():
+        if rec and rec.get("source_digest") == source_digest(mx):
             return int(rec["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -154,8 +172,9 @@ def one_per_expert_inputs(cfg):
     return x, rw, np.zeros(cfg.E, np.uint16)
 
 
-def build_layer(cfg, device, routing="synthetic"):
-    """Inputs of the workload resident on the device; weights packed by the library."""
+def build_layer(cfg, device, routing="synthetic", mx=False):
+    """Inputs of the workload resident on the device; weights packed by the library
+    (mx: MXFP8 codes and scale atoms)."""
     import torch
     import sparse_moe_layer_gb300 as moe
 
@@ -170,22 +189,48 @@ def build_layer(cfg, device, routing="synthetic"):
     b13, b2 = synth.expert_biases(cfg)
     E, H, I, Hp, Ip = cfg.E, cfg.H, cfg.I, cfg.Hp, cfg.Ip
     w13 = torch.empty(moe.w13_shape(E, H, I), dtype=torch.uint8, device=device)
-    s13 = torch.empty((E, 2 * Ip // 128, Hp // 128), dtype=torch.float32, device=device)
     w2 = torch.empty(moe.w2_shape(E, H, I), dtype=torch.uint8, device=device)
-    s2 = torch.empty((E, Hp // 128, Ip // 128), dtype=torch.float32, device=device)
+    if mx:
+        s13 = torch.empty(moe.s13_mx_shape(E, H, I), dtype=torch.uint8, device=device)
+        s2 = torch.empty(moe.s2_mx_shape(E, H, I), dtype=torch.uint8, device=device)
+    else:
+        s13 = torch.empty((E, 2 * Ip // 128, Hp // 128), dtype=torch.float32, device=device)
+        s2 = torch.empty((E, Hp // 128, Ip // 128), dtype=torch.float32, device=device)
+    pack = moe.pack_weights_into_mx if mx else moe.pack_weights_into
     chunk = 8
     for e0 in range(0, E, chunk):
         n = min(chunk, E - e0)
         m13 = torch.from_numpy(synth.w13_master(cfg, e0, n)).to(device)
         m2 = torch.from_numpy(synth.w2_master(cfg, e0, n)).to(device)
-        moe.pack_weights_into(m13, m2, H, I, n, w13[e0:e0 + n], s13[e0:e0 + n], w2[e0:e0 + n], s2[e0:e0 + n])
+        pack(m13, m2, H, I, n, w13[e0:e0 + n], s13[e0:e0 + n], w2[e0:e0 + n], s2[e0:e0 + n])
         torch.cuda.synchronize()
         del m13, m2
     layer = moe.MoeLayer(bf16(rw), bf16(rb), w13, s13, bf16(b13), w2, s2, bf16(b2), cfg.top_k)
     return layer, bf16(x), x
 
 
-def cpu_oracle_leg(cfg, seconds: float):
+def oracle_format(cfg, mx: bool):
+    """Empty oracle weight arrays of the format, its per-expert packer and its layer forward."""
+    import oracle
+    E, Hp, Ip = cfg.E, cfg.Hp, cfg.Ip
+    if mx:
+        arrs = (np.zeros((E, 2 * Ip, Hp), np.uint8), np.zeros((E, 2 * Ip, Hp // 32), np.uint8),
+                np.zeros((E, Hp, Ip), np.uint8), np.zeros((E, Hp, Ip // 32), np.uint8))
+        p13, p2, fwd = oracle.mx_pack_w13, oracle.mx_pack_w2, oracle.mx_forward
+    else:
+        arrs = (np.zeros((E, 2 * Ip, Hp), np.uint8), np.ones((E, 2 * Ip // 128, Hp // 128), np.float32),
+                np.zeros((E, Hp, Ip), np.uint8), np.ones((E, Hp // 128, Ip // 128), np.float32))
+        p13, p2, fwd = oracle.pack_w13, oracle.pack_w2, oracle.forward
+    q13, s13, q2, s2 = arrs
+
+    def pack(e):
+        p13(synth.w13_master(cfg, int(e), 1), q13[e:e + 1], s13[e:e + 1])
+        p2(synth.w2_master(cfg, int(e), 1), q2[e:e + 1], s2[e:e + 1])
+
+    return arrs, pack, fwd
+
+
+def cpu_oracle_leg(cfg, seconds: float, mx: bool = False):
     """Time the oracle (single thread) on a bounded sample of the workload:
     about `seconds` of CPU work -- the tokens of a fixed random sample (at most
     the whole batch), the full layer per token, repeated if one pass is short.
@@ -196,22 +241,13 @@ def cpu_oracle_leg(cfg, seconds: float):
     b13, b2 = synth.expert_biases(cfg)
     k = cfg.top_k
     order = np.random.default_rng(1234).permutation(cfg.T).astype(np.int32)
-    E, Hp, Ip = cfg.E, cfg.Hp, cfg.Ip
-    q13 = np.zeros((E, 2 * Ip, Hp), np.uint8)
-    s13 = np.ones((E, 2 * Ip // 128, Hp // 128), np.float32)
-    q2 = np.zeros((E, Hp, Ip), np.uint8)
-    s2 = np.ones((E, Hp // 128, Ip // 128), np.float32)
+    (q13, s13, q2, s2), pack, fwd = oracle_format(cfg, mx)
     packed = set()
     from concurrent.futures import ThreadPoolExecutor
 
     def pack_for(tokens):  # weight conversion is offline for both sides: untimed
         r = oracle.router(np.ascontiguousarray(x[tokens]), rw, rb, k)
         todo = [int(e) for e in np.unique(r["idx"]) if int(e) not in packed]
-
-        def pack(e):
-            oracle.pack_w13(synth.w13_master(cfg, e, 1), q13[e:e + 1], s13[e:e + 1])
-            oracle.pack_w2(synth.w2_master(cfg, e, 1), q2[e:e + 1], s2[e:e + 1])
-
         with ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
             list(ex.map(pack, todo))
         packed.update(todo)
@@ -220,7 +256,7 @@ def cpu_oracle_leg(cfg, seconds: float):
     probe = np.sort(order[:min(2, cfg.T)])
     pack_for(probe)
     t0 = time.perf_counter()
-    oracle.forward(x, rw, rb, q13, s13, b13, q2, s2, b2, k, tokens=probe)
+    fwd(x, rw, rb, q13, s13, b13, q2, s2, b2, k, tokens=probe)
     per_token = max((time.perf_counter() - t0) / len(probe), 1e-6)
     n = int(min(cfg.T, max(1, seconds / per_token)))
     passes = max(1, int(seconds / (n * per_token)))
@@ -228,10 +264,10 @@ def cpu_oracle_leg(cfg, seconds: float):
     pack_for(tokens)
     t0 = time.perf_counter()
     for _ in range(passes):
-        oracle.forward(x, rw, rb, q13, s13, b13, q2, s2, b2, k, tokens=tokens)
+        fwd(x, rw, rb, q13, s13, b13, q2, s2, b2, k, tokens=tokens)
     dt = time.perf_counter() - t0
     desc = (f"{n} of {cfg.T} tokens x {passes} pass(es) ({len(packed)} experts), full layer per token, "
-            f"single-threaded fp64 oracle")
+            f"single-threaded fp64 oracle" + (" (MXFP8 variant)" if mx else ""))
     return passes * n / dt, desc, dt
 
 
@@ -247,24 +283,16 @@ def run_reference(args, cfg, rank):
     rng = np.random.default_rng(99)
     tokens_all = rng.permutation(cfg.T).astype(np.int32)
     r = oracle.router(np.ascontiguousarray(x[tokens_all]), rw, rb, k)
-    E, Hp, Ip = cfg.E, cfg.Hp, cfg.Ip
-    q13 = np.zeros((E, 2 * Ip, Hp), np.uint8)
-    s13 = np.ones((E, 2 * Ip // 128, Hp // 128), np.float32)
-    q2 = np.zeros((E, Hp, Ip), np.uint8)
-    s2 = np.ones((E, Hp // 128, Ip // 128), np.float32)
+    mx = args.format == "mx"
+    (q13, s13, q2, s2), pack, fwd = oracle_format(cfg, mx)
     from concurrent.futures import ThreadPoolExecutor
     needed = np.unique(r["idx"])
-
-    def pack(e):
-        oracle.pack_w13(synth.w13_master(cfg, int(e), 1), q13[e:e + 1], s13[e:e + 1])
-        oracle.pack_w2(synth.w2_master(cfg, int(e), 1), q2[e:e + 1], s2[e:e + 1])
-
     with ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
         list(ex.map(pack, needed))
     # one token per step, cycling through a seeded permutation of the batch
     def step(i):
         t = tokens_all[i % len(tokens_all)]
-        oracle.forward(x, rw, rb, q13, s13, b13, q2, s2, b2, k, tokens=np.array([t], np.int32))
+        fwd(x, rw, rb, q13, s13, b13, q2, s2, b2, k, tokens=np.array([t], np.int32))
 
     for i in range(args.warmup):
         step(i)
@@ -276,7 +304,8 @@ def run_reference(args, cfg, rank):
     line = dict(metric=METRIC, value=value, unit="tokens/s", n_gpus=args.gpus, steps=args.steps, warmup=args.warmup,
                 ms_per_step=dt * 1e3 / args.steps, higher_is_better=True, scaling="weak", vs_baseline=None,
                 dtype="f64", data="synthetic", impl="reference",
-                config=dict(workload=workload_str(cfg), step="one token of the batch through the whole layer"),
+                config=dict(workload=workload_str(cfg), step="one token of the batch through the whole layer",
+                            weights=WEIGHTS[args.format]),
                 cpu_baseline=dict(value=value, unit="tokens/s", cores=1, kind="oracle",
                                   sample=f"{args.steps} tokens, one per step, single-threaded fp64 C oracle"),
                 e2e=dict(value=value, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
@@ -290,6 +319,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=[c.name for c in synth.CONFIGS])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--format", default="block128", choices=["block128", "mx"],
+                    help="mx: the MXFP8 variant (moe_forward_mx)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work in the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
@@ -326,7 +357,8 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    layer, x_dev, x_host_np = build_layer(cfg, dev, args.routing)
+    mx = args.format == "mx"
+    layer, x_dev, x_host_np = build_layer(cfg, dev, args.routing, mx)
     T, H = cfg.T, cfg.H
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -338,8 +370,8 @@ def main():
     torch.cuda.synchronize()
     ws = layer.workspace(T)
     assert moe.read_device_status(ws) == 0, "device wait timed out during warm-up"
-    counts = moe.workspace_views(ws, T, cfg.H, cfg.I, cfg.E, cfg.top_k)["count"].cpu().numpy()
-    alg = algorithmic(cfg, counts)
+    counts = moe.workspace_views(ws, T, cfg.H, cfg.I, cfg.E, cfg.top_k, mx=mx)["count"].cpu().numpy()
+    alg = algorithmic(cfg, counts, mx)
 
     K = args.steps
     # Timed region 1 (the value): the step replayed as a CUDA graph (one memset
@@ -439,9 +471,13 @@ def main():
     else:
         roof = dict(bound="hbm", achieved=alg["gemm1_bytes"] / g1_s / 1e9, peak=pk["hbm"], unit="GB/s")
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = recorded_traffic("gemm_gateup", cfg.name)
-    roof["kernel"] = ("moe_gemm_kernel<true> (gate/up GEMM + SwiGLU + requant)" if prefill else
-                      "moe_gemm_decode_kernel<true> (swap-AB gate/up GEMM + SwiGLU + requant)")
+    roof["traffic"] = recorded_traffic("gemm_gateup_mx" if mx else "gemm_gateup", cfg.name, mx)
+    if mx:
+        roof["kernel"] = ("moe_gemm_mx_kernel<true> (block-scaled gate/up GEMM + SwiGLU + MX requant)" if prefill else
+                          "moe_gemm_mx_decode_kernel<true> (swap-AB block-scaled gate/up GEMM + SwiGLU + MX requant)")
+    else:
+        roof["kernel"] = ("moe_gemm_kernel<true> (gate/up GEMM + SwiGLU + requant)" if prefill else
+                          "moe_gemm_decode_kernel<true> (swap-AB gate/up GEMM + SwiGLU + requant)")
     roof["peak_source"] = pk["source"] + (" (hbm_gbs)" if not prefill else " (2 x bf16_tflops_sustained)")
     roof["algorithmic_per_launch"] = alg["gemm1_bytes"] if not prefill else alg["gemm1_flops"]
 
@@ -453,20 +489,23 @@ def main():
                                                           " routing=one row per expert (T = E/top_k)"),
                             parallelism=f"replicas{world}",
                             l2="flushed before every step (256 MiB write, outside the timed events)",
-                            weights="FP8 e4m3 128x128 block scales, packed on device by moe_pack_weights"),
+                            weights=WEIGHTS[args.format]),
                 roofline=roof,
                 step=dict(ms_per_stage=stage_ms, active_experts=alg["active"],
+                          gemm_down_achieved=(alg["gemm2_flops"] / (stage_ms["gemm_down"] * 1e-3) / 1e12 if prefill
+                                              else alg["gemm2_bytes"] / (stage_ms["gemm_down"] * 1e-3) / 1e9),
                           step_GBps=alg["step_bytes"] / (ms * 1e-3) / 1e9,
                           step_hbm_frac=alg["step_bytes"] / (ms * 1e-3) / 1e9 / pk["hbm"],
                           gemm_tflops=(alg["gemm1_flops"] + alg["gemm2_flops"]) / (ms * 1e-3) / 1e12,
-                          wall_s=wall, device_status=status, launch="CUDA graph replay of moe_forward",
+                          wall_s=wall, device_status=status,
+                          launch="CUDA graph replay of " + ("moe_forward_mx" if mx else "moe_forward"),
                           eager_ms_per_step=eager_ms),
                 e2e=dict(value=world * T / (e2e_ms * 1e-3), unit="tokens/s", h2d_bytes_per_step=T * H * 2,
                          d2h_bytes_per_step=T * H * 2, ms_per_step=e2e_ms),
                 gpu_launches=5 * K,
                 clocks=sampler.summary())
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, desc, dt = cpu_oracle_leg(cfg, args.cpu_seconds)
+        v, desc, dt = cpu_oracle_leg(cfg, args.cpu_seconds, mx)
         line["cpu_baseline"] = dict(value=v, unit="tokens/s", cores=1, kind="oracle", sample=desc, seconds=dt)
     if rank == 0:
         print(json.dumps(line), flush=True)

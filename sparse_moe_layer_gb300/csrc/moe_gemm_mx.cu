@@ -75,8 +75,9 @@ struct MxCfg {
     static constexpr int SF_COL0 = BN;                 // TMEM: accumulator [0, 256), scale ring after it
     static constexpr int SF_STRIDE = 16;               // TMEM columns per stage (three 4-column atoms)
     static constexpr int TMEM_COLS = 512;
-    static constexpr int EPI_WARPS = 8;
-    static constexpr int THREADS = (4 + EPI_WARPS) * 32;
+    static constexpr int EPI_WARP0 = 4;  // warps 0-3: producer, MMA issuer, metadata, idle
+    static constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter (warp & 3)
+    static constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
     static constexpr int SMEM_BYTES = STAGES * (STAGE_BYTES + SF_BYTES) + 1024;
     static constexpr uint32_t IDESC = idesc_mx_e4m3(BM, BN);
     static_assert(SF_COL0 + STAGES * SF_STRIDE <= TMEM_COLS, "scale ring does not fit in TMEM");
@@ -106,6 +107,9 @@ __global__ void __launch_bounds__(MxCfg<GATED>::THREADS, 1)
     __shared__ float s_bias[2][C::BN];
     __shared__ int s_rslot[2][GATED ? 1 : 128];
     __shared__ float s_rw[2][GATED ? 1 : 128];
+    // down GEMM: per epilogue warp, 32 rows x 16 fp32 (+4 pad: conflict-free
+    // 16-byte accesses) that turn row-per-lane results into 64-byte row segments
+    __shared__ __align__(16) float s_stage[GATED ? 1 : C::EPI_WARPS][32][20];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = p.E;
@@ -274,10 +278,10 @@ __global__ void __launch_bounds__(MxCfg<GATED>::THREADS, 1)
             }
             mbar_arrive(smem_u32(&bfull_bar[slot]));
         }
-    } else if (warp >= 4) {
+    } else if (warp >= C::EPI_WARP0) {
         // --------------------------------------------------------- epilogue
-        const int quarter = warp & 3;       // TMEM lanes this warp may access
-        const int half = (warp - 4) >> 2;   // which 64 columns of each 128-column block
+        const int quarter = warp & 3;                   // TMEM lanes this warp may access
+        const int half = (warp - C::EPI_WARP0) >> 2;    // which 64 columns of each 128-column block
         const int row = quarter * 32 + lane;
         const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
         uint32_t dphase = 0;
@@ -346,17 +350,35 @@ __global__ void __launch_bounds__(MxCfg<GATED>::THREADS, 1)
                     *reinterpret_cast<uint16_t*>(p.sh + ((size_t)mtid * (p.ldq / 128) + ti.nt) * kMxAtomBytes +
                                                  mx_atom_byte(row, 2 * half)) = (uint16_t)bytes;
             } else {
+                // w * y rows to part[slot, :].  A lane holds one row, so direct stores
+                // would write 16 bytes into each of 32 rows per instruction; instead
+                // each 32-row x 16-column chunk goes through shared memory and leaves
+                // as 64-byte row segments, 8 rows per instruction.
                 const bool has1 = 2 * ti.nt + 1 < p.sw_rowblocks;
-                if (valid) {
+                float (*stage)[20] = s_stage[GATED ? 0 : warp - C::EPI_WARP0];
+                const int sr = lane >> 2, sq = lane & 3;  // store phase: rows sr + 8i, 16-byte piece sq
+                // invalid rows (past the tile's rows) get slot -1 and are skipped
+                const int slot_or_skip = valid ? my_slot : -1;
 #pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        if (b == 1 && !has1) break;
-                        float4* dst = reinterpret_cast<float4*>(p.part + (size_t)my_slot * p.ldp +
-                                                                (2 * ti.nt + b) * 128 + 64 * half);
+                for (int b = 0; b < 2; ++b) {
+                    if (b == 1 && !has1) break;
 #pragma unroll
-                        for (int v = 0; v < 16; ++v)
-                            dst[v] = make_float4(my_w * acc[64 * b + 4 * v], my_w * acc[64 * b + 4 * v + 1],
-                                                 my_w * acc[64 * b + 4 * v + 2], my_w * acc[64 * b + 4 * v + 3]);
+                    for (int c = 0; c < 4; ++c) {
+                        float4* srow = reinterpret_cast<float4*>(&stage[lane][0]);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int i = 64 * b + 16 * c + 4 * v;
+                            srow[v] = make_float4(my_w * acc[i], my_w * acc[i + 1], my_w * acc[i + 2], my_w * acc[i + 3]);
+                        }
+                        __syncwarp();
+                        const int col = (2 * ti.nt + b) * 128 + 64 * half + 16 * c + 4 * sq;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int st = __shfl_sync(0xffffffffu, slot_or_skip, sr + 8 * i);
+                            const float4 v = *reinterpret_cast<const float4*>(&stage[sr + 8 * i][4 * sq]);
+                            if (st >= 0) *reinterpret_cast<float4*>(p.part + (size_t)st * p.ldp + col) = v;
+                        }
+                        __syncwarp();
                     }
                 }
             }

@@ -353,6 +353,7 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
     __shared__ int s_row[8 * kMaxTopK];
     __shared__ int s_eoff[kMaxExperts];  // MXFP8: first row of each expert ...
     __shared__ int s_emt[kMaxExperts];   // ... and the m-tiles of the experts before it
+    __shared__ long long s_aoff[8 * kMaxTopK];  // MXFP8: byte offset of each row's cell in K block 0's atom
     const int tpc = p.tokens_per_cta;
     const int t0 = blockIdx.x * tpc;
     const int chunk = t0 / kChunkTokens;
@@ -457,6 +458,11 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
         for (int u = 0; u < tt; ++u)
             for (int jj = 0; jj < p.k; ++jj) r += (s_idx[u * p.k + jj] == e);
         s_row[i] = r;
+        if (p.mx) {
+            const int local = r - s_eoff[e];
+            const int mt = s_emt[e] + local / p.bm, m = local - (local / p.bm) * p.bm;
+            s_aoff[i] = (long long)mt * (p.Hp / 128) * kMxAtomBytes + mx_atom_byte(m, 0);
+        }
         int slot = (t0 + tt) * p.k + j;
         p.perm[r] = slot;
         p.inv[slot] = r;
@@ -492,13 +498,8 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
             for (int j = 0; j < p.k; ++j) {
                 const int r = s_row[tt * p.k + j];
                 *reinterpret_cast<uint32_t*>(p.xq + (size_t)r * p.Hp + c) = q;
-                if (lane == 0) {
-                    const int e = s_idx[tt * p.k + j];
-                    const int local = r - s_eoff[e];
-                    const int mt = s_emt[e] + local / p.bm, m = local % p.bm;
-                    *reinterpret_cast<uint32_t*>(p.sxa + ((size_t)mt * G + g) * kMxAtomBytes + mx_atom_byte(m, 0)) =
-                        cell;
-                }
+                if (lane == 0)
+                    *reinterpret_cast<uint32_t*>(p.sxa + s_aoff[tt * p.k + j] + (size_t)g * kMxAtomBytes) = cell;
             }
             continue;
         }
