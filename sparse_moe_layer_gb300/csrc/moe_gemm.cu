@@ -123,6 +123,9 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
     __shared__ float s_sw01[2][4];
     __shared__ int s_rslot[2][GATED ? 1 : 128];
     __shared__ float s_rw[2][GATED ? 1 : 128];
+    // down GEMM: per epilogue warp, 32 rows x 16 fp32 (+4 pad: conflict-free
+    // 16-byte accesses) that turn row-per-lane results into 64-byte row segments
+    __shared__ __align__(16) float s_stage[GATED ? 1 : C::EPI_WARPS][32][20];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = p.E;
@@ -424,17 +427,33 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                     if (half == 0) p.sh[(size_t)ti.nt * p.R + grow] = s;
                 }
             } else {
-                if (valid) {
-                    const float w = my_w;
+                // w * y rows to part[slot, :].  A lane holds one row, so direct stores
+                // would write 16 bytes into each of 32 rows per instruction; instead
+                // each 32-row x 16-column chunk goes through shared memory and leaves
+                // as 64-byte row segments, 8 rows per instruction.
+                float (*stage)[20] = s_stage[GATED ? 0 : ew];
+                const int sr = lane >> 2, sq = lane & 3;  // store phase: rows sr + 8i, 16-byte piece sq
+                const int slot_or_skip = valid ? my_slot : -1;  // rows past the tile's rows are skipped
 #pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        if (b == 1 && !has1) break;
-                        float4* dst =
-                            reinterpret_cast<float4*>(p.part + (size_t)my_slot * p.ldp + (2 * ti.nt + b) * 128 + 64 * half);
+                for (int b = 0; b < 2; ++b) {
+                    if (b == 1 && !has1) break;
 #pragma unroll
-                        for (int v = 0; v < 16; ++v)
-                            dst[v] = make_float4(w * acc[64 * b + 4 * v], w * acc[64 * b + 4 * v + 1],
-                                                 w * acc[64 * b + 4 * v + 2], w * acc[64 * b + 4 * v + 3]);
+                    for (int c = 0; c < 4; ++c) {
+                        float4* srow = reinterpret_cast<float4*>(&stage[lane][0]);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int i = 64 * b + 16 * c + 4 * v;
+                            srow[v] = make_float4(my_w * acc[i], my_w * acc[i + 1], my_w * acc[i + 2], my_w * acc[i + 3]);
+                        }
+                        __syncwarp();
+                        const int col = (2 * ti.nt + b) * 128 + 64 * half + 16 * c + 4 * sq;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int st = __shfl_sync(0xffffffffu, slot_or_skip, sr + 8 * i);
+                            const float4 v = *reinterpret_cast<const float4*>(&stage[sr + 8 * i][4 * sq]);
+                            if (st >= 0) *reinterpret_cast<float4*>(p.part + (size_t)st * p.ldp + col) = v;
+                        }
+                        __syncwarp();
                     }
                 }
             }
