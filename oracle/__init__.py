@@ -57,9 +57,18 @@ def lib():
         L.oracle_mx_pack_w13.argtypes = [vp, i32, i32, i32, vp, vp]
         L.oracle_mx_pack_w2.argtypes = [vp, i32, i32, i32, vp, vp]
         L.oracle_mx_forward.argtypes = [vp] * 9 + [i32] * 5 + [vp, i32, vp, vp, vp, vp, vp]
+        L.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+        L.oracle_e2m1_decode.restype = f64
+        L.oracle_e2m1_encode.argtypes = [f32]
+        L.oracle_e2m1_encode.restype = ctypes.c_uint8
+        L.oracle_mx4_quant_rows_f32.argtypes = [vp, i32, i32, vp, vp]
+        L.oracle_mx4_pack_w13.argtypes = [vp, i32, i32, i32, vp, vp]
+        L.oracle_mx4_pack_w2.argtypes = [vp, i32, i32, i32, vp, vp]
+        L.oracle_mx4_forward.argtypes = [vp] * 9 + [i32] * 5 + [vp, i32, vp, vp, vp, vp, vp]
         for f in ("oracle_quant_rows_bf16", "oracle_quant_rows_f32", "oracle_pack_w13", "oracle_pack_w2",
                   "oracle_router", "oracle_permute", "oracle_forward", "oracle_mx_quant_rows_f32",
-                  "oracle_mx_quant_rows_bf16", "oracle_mx_pack_w13", "oracle_mx_pack_w2", "oracle_mx_forward"):
+                  "oracle_mx_quant_rows_bf16", "oracle_mx_pack_w13", "oracle_mx_pack_w2", "oracle_mx_forward",
+                  "oracle_mx4_quant_rows_f32", "oracle_mx4_pack_w13", "oracle_mx4_pack_w2", "oracle_mx4_forward"):
             getattr(L, f).restype = None
         _lib = L
     return _lib
@@ -234,9 +243,11 @@ def mx_pack_w2(w2: np.ndarray, q: np.ndarray | None = None, s: np.ndarray | None
     return q, s
 
 
-def mx_forward(x, rw, rb, w13, s13, b13, w2, s2, b2, k: int, tokens=None, want_intermediates: bool = False):
+def mx_forward(x, rw, rb, w13, s13, b13, w2, s2, b2, k: int, tokens=None, want_intermediates: bool = False,
+               weights: str = "mxfp8"):
     """Layer output rows (bf16 bits) of the MXFP8 variant; arguments as forward()
-    with MX codes and scale bytes (s13 [E, 2Ip, Hp/32], s2 [E, Hp, Ip/32])."""
+    with MX codes and scale bytes (s13 [E, 2Ip, Hp/32], s2 [E, Hp, Ip/32]).
+    weights="mxfp4": the weight codes are E2M1 (one per byte, from mx4_pack_*)."""
     T, H = x.shape
     E = rw.shape[0]
     I = b13.shape[1] // 2
@@ -248,7 +259,8 @@ def mx_forward(x, rw, rb, w13, s13, b13, w2, s2, b2, k: int, tokens=None, want_i
     sh = np.empty((n * k, Ip // 32), np.uint8) if want_intermediates else None
     y = np.empty((n * k, H), np.float64) if want_intermediates else None
     ids = np.empty(n * k, np.int32) if want_intermediates else None
-    lib().oracle_mx_forward(_p(np.ascontiguousarray(x, np.uint16)), _p(np.ascontiguousarray(rw, np.uint16)),
+    fwd = lib().oracle_mx4_forward if weights == "mxfp4" else lib().oracle_mx_forward
+    fwd(_p(np.ascontiguousarray(x, np.uint16)), _p(np.ascontiguousarray(rw, np.uint16)),
                             _p(np.ascontiguousarray(rb, np.uint16)), _p(w13), _p(s13),
                             _p(np.ascontiguousarray(b13, np.uint16)), _p(w2), _p(s2),
                             _p(np.ascontiguousarray(b2, np.uint16)), T, H, I, E, k, _p(tok), n, _p(out), _p(hq),
@@ -256,3 +268,49 @@ def mx_forward(x, rw, rb, w13, s13, b13, w2, s2, b2, k: int, tokens=None, want_i
     if want_intermediates:
         return out, dict(hq=hq, sh=sh, y=y, idx=ids)
     return out
+
+
+# ---- MXFP4 weights (E2M1 codes, one per byte) ----
+def e2m1_decode(c: int) -> float:
+    return float(lib().oracle_e2m1_decode(int(c)))
+
+
+def e2m1_encode(v: float) -> int:
+    return int(lib().oracle_e2m1_encode(float(v)))
+
+
+def mx4_quant_rows_f32(x: np.ndarray):
+    """fp32 [rows, cols] -> E2M1 codes [rows, Cp] (one per byte), scale bytes [rows, Cp/32]."""
+    rows, cols = x.shape
+    cp = _pad128(cols)
+    q = np.empty((rows, cp), np.uint8)
+    s = np.empty((rows, cp // 32), np.uint8)
+    lib().oracle_mx4_quant_rows_f32(_p(np.ascontiguousarray(x, np.float32)), rows, cols, _p(q), _p(s))
+    return q, s
+
+
+def mx4_pack_w13(w13: np.ndarray, q: np.ndarray | None = None, s: np.ndarray | None = None):
+    """fp32 [n, 2I, H] -> E2M1 codes [n, 2Ip, Hp], scale bytes [n, 2Ip, Hp/32]."""
+    n, twoI, H = w13.shape
+    I = twoI // 2
+    Hp, Ip = _pad128(H), _pad128(I)
+    q = np.empty((n, 2 * Ip, Hp), np.uint8) if q is None else q
+    s = np.empty((n, 2 * Ip, Hp // 32), np.uint8) if s is None else s
+    lib().oracle_mx4_pack_w13(_p(np.ascontiguousarray(w13, np.float32)), H, I, n, _p(q), _p(s))
+    return q, s
+
+
+def mx4_pack_w2(w2: np.ndarray, q: np.ndarray | None = None, s: np.ndarray | None = None):
+    """fp32 [n, H, I] -> E2M1 codes [n, Hp, Ip], scale bytes [n, Hp, Ip/32]."""
+    n, H, I = w2.shape
+    Hp, Ip = _pad128(H), _pad128(I)
+    q = np.empty((n, Hp, Ip), np.uint8) if q is None else q
+    s = np.empty((n, Hp, Ip // 32), np.uint8) if s is None else s
+    lib().oracle_mx4_pack_w2(_p(np.ascontiguousarray(w2, np.float32)), H, I, n, _p(q), _p(s))
+    return q, s
+
+
+def mx4_forward(x, rw, rb, w13, s13, b13, w2, s2, b2, k: int, tokens=None, want_intermediates: bool = False):
+    """The layer with MXFP4 weights and MXFP8 activations (see mx_forward)."""
+    return mx_forward(x, rw, rb, w13, s13, b13, w2, s2, b2, k, tokens=tokens, want_intermediates=want_intermediates,
+                      weights="mxfp4")

@@ -534,41 +534,44 @@ void oracle_mx_pack_w2(const float* w2, int H, int I, int n_exp, uint8_t* q, uin
 /* sum over 32-groups g of 2^(sa[g]-127) * 2^(sw[n,g]-127) * sum_{i in g}
  * dec(a[i]) * dec(w[n,i]), in fp64 (exact: e4m3 products and their sums over
  * 32 fit in fp64, the scales are powers of two). */
-static double mx_dot(const uint8_t* a, const uint8_t* sa, const uint8_t* w, const uint8_t* sw, int n, int Kp) {
+static double mx_dot(const uint8_t* a, const uint8_t* sa, const uint8_t* w, const uint8_t* sw, int n, int Kp,
+                     const double* wtab) {
     int G = Kp / 32;
     double acc = 0.0;
     for (int g = 0; g < G; ++g) {
         double part = 0.0;
-        for (int i = g * 32; i < g * 32 + 32; ++i) part += E4M3[a[i]] * E4M3[w[(size_t)n * Kp + i]];
+        for (int i = g * 32; i < g * 32 + 32; ++i) part += E4M3[a[i]] * wtab[w[(size_t)n * Kp + i]];
         acc += ldexp(part, ((int)sa[g] - 127) + ((int)sw[(size_t)n * G + g] - 127));
     }
     return acc;
 }
 
+/* wtab: decode table of the weight codes (E4M3 for MXFP8 weights, E2M1 for
+ * MXFP4 weights); activations are MXFP8 either way. */
 static void mx_expert_ffn(const uint8_t* xq, const uint8_t* sx, const uint8_t* w13e, const uint8_t* s13e,
                           const uint16_t* b13e, const uint8_t* w2e, const uint8_t* s2e, const uint16_t* b2e, int H,
-                          int I, uint8_t* hq, uint8_t* sh, double* y) {
+                          int I, uint8_t* hq, uint8_t* sh, double* y, const double* wtab) {
     int Hp = (H + 127) / 128 * 128, Ip = (I + 127) / 128 * 128;
     float* h = (float*)malloc(sizeof(float) * (size_t)I);
     for (int n = 0; n < I; ++n) {
-        double g = (double)bf16_value(b13e[n]) + mx_dot(xq, sx, w13e, s13e, n, Hp);
-        double u = (double)bf16_value(b13e[I + n]) + mx_dot(xq, sx, w13e, s13e, Ip + n, Hp);
+        double g = (double)bf16_value(b13e[n]) + mx_dot(xq, sx, w13e, s13e, n, Hp, wtab);
+        double u = (double)bf16_value(b13e[I + n]) + mx_dot(xq, sx, w13e, s13e, Ip + n, Hp, wtab);
         double silu = g / (1.0 + exp(-g));
         h[n] = (float)(silu * u);
     }
     oracle_mx_quant_rows_f32(h, 1, I, hq, sh);
     free(h);
-    for (int n = 0; n < H; ++n) y[n] = (double)bf16_value(b2e[n]) + mx_dot(hq, sh, w2e, s2e, n, Ip);
+    for (int n = 0; n < H; ++n) y[n] = (double)bf16_value(b2e[n]) + mx_dot(hq, sh, w2e, s2e, n, Ip, wtab);
 }
 
 /* The layer with MXFP8 quantisation; arguments as oracle_forward, with the
  * scale arrays in UE8M0 bytes (s13 [E, 2Ip, Hp/32], s2 [E, Hp, Ip/32]) and
  * sh_rows [ntok*k, Ip/32]. */
-void oracle_mx_forward(const uint16_t* x, const uint16_t* rw, const uint16_t* rb, const uint8_t* w13,
-                       const uint8_t* s13, const uint16_t* b13, const uint8_t* w2, const uint8_t* s2,
-                       const uint16_t* b2, int T, int H, int I, int E, int k, const int32_t* tokens, int ntok,
-                       uint16_t* out_rows, uint8_t* hq_rows, uint8_t* sh_rows, double* y_rows, int32_t* idx_rows) {
-    e4m3_init();
+static void mx_forward_impl(const uint16_t* x, const uint16_t* rw, const uint16_t* rb, const uint8_t* w13,
+                            const uint8_t* s13, const uint16_t* b13, const uint8_t* w2, const uint8_t* s2,
+                            const uint16_t* b2, int T, int H, int I, int E, int k, const int32_t* tokens, int ntok,
+                            uint16_t* out_rows, uint8_t* hq_rows, uint8_t* sh_rows, double* y_rows, int32_t* idx_rows,
+                            const double* wtab) {
     int Hp = (H + 127) / 128 * 128, Ip = (I + 127) / 128 * 128;
     if (!tokens) ntok = T;
     double* logits = (double*)malloc(sizeof(double) * (size_t)E);
@@ -591,7 +594,7 @@ void oracle_mx_forward(const uint16_t* x, const uint16_t* rw, const uint16_t* rb
             int e = idx[j];
             mx_expert_ffn(xq, sx, w13 + (size_t)e * 2 * Ip * Hp, s13 + (size_t)e * 2 * Ip * (Hp / 32),
                           b13 + (size_t)e * 2 * I, w2 + (size_t)e * Hp * Ip, s2 + (size_t)e * Hp * (Ip / 32),
-                          b2 + (size_t)e * H, H, I, hq, sh, y);
+                          b2 + (size_t)e * H, H, I, hq, sh, y, wtab);
             double wj = bf16_value(wb[j]);
             for (int n = 0; n < H; ++n) acc[n] += wj * y[n];
             size_t row = (size_t)i * k + j;
@@ -609,4 +612,145 @@ void oracle_mx_forward(const uint16_t* x, const uint16_t* rw, const uint16_t* rb
     free(sh);
     free(y);
     free(acc);
+}
+
+void oracle_mx_forward(const uint16_t* x, const uint16_t* rw, const uint16_t* rb, const uint8_t* w13,
+                       const uint8_t* s13, const uint16_t* b13, const uint8_t* w2, const uint8_t* s2,
+                       const uint16_t* b2, int T, int H, int I, int E, int k, const int32_t* tokens, int ntok,
+                       uint16_t* out_rows, uint8_t* hq_rows, uint8_t* sh_rows, double* y_rows, int32_t* idx_rows) {
+    e4m3_init();
+    mx_forward_impl(x, rw, rb, w13, s13, b13, w2, s2, b2, T, H, I, E, k, tokens, ntok, out_rows, hq_rows, sh_rows,
+                    y_rows, idx_rows, E4M3);
+}
+
+/* ------------------------------------------------------------------ */
+/* MXFP4 weights                                                      */
+/* ------------------------------------------------------------------ */
+/* "GPT-OSS on Day 0" (opening section): the open-weight models ship with
+ * MXFP4 quantisation, and the FP4 tensor cores that run it natively are new
+ * with Blackwell.  OCP Microscaling Formats (MX) v1.0: the element format is
+ * FP4 E2M1 (section 5.3.3: 1 sign bit, 2 exponent bits with bias 1, 1
+ * mantissa bit, no infinities or NaN; exponent field 0 is subnormal, m * 0.5;
+ * otherwise (1 + m/2) * 2^(e-1): magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), the
+ * block is 32 values with one UE8M0 scale, and the shared exponent is
+ * X = floor(log2(amax)) - 2 (section 6.3; 2 = the exponent of E2M1's largest
+ * normal).  Codes: e2m1(v / 2^X), nearest, ties to the even code, saturating
+ * to +-6 (values of the top binade above 6).  The readings of the MXFP8
+ * section carry over (all-zero group: byte 0 and +0 codes; X clamped to
+ * [-127, 127]).  The layer: weights in MXFP4 along K, x and h in MXFP8 --
+ * FP4 codes with FP8 activations.  Codes are kept one per byte here (the low
+ * 4 bits: sign in bit 3). */
+static double E2M1[16];
+static int e2m1_ready = 0;
+
+static void e2m1_init(void) {
+    if (e2m1_ready) return;
+    for (int c = 0; c < 16; ++c) {
+        int sgn = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+        double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+        E2M1[c] = sgn ? -v : v;
+    }
+    e2m1_ready = 1;
+}
+
+double oracle_e2m1_decode(uint8_t c) {
+    e2m1_init();
+    return E2M1[c & 15];
+}
+
+/* Nearest E2M1 code of an fp32 value, ties to the even code (even mantissa
+ * bit), saturating to +-6; the sign is kept for values that round to 0. */
+uint8_t oracle_e2m1_encode(float v) {
+    e2m1_init();
+    double a = fabs((double)v);
+    uint8_t sgn = signbit(v) ? 8 : 0;
+    int c;
+    if (a >= E2M1[7]) {
+        c = 7;
+    } else {
+        int lo = 0, hi = 7; /* E2M1[lo] <= a < E2M1[hi] */
+        while (hi - lo > 1) {
+            int mid = (lo + hi) / 2;
+            if (E2M1[mid] <= a)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        double dl = a - E2M1[lo], dh = E2M1[hi] - a;
+        c = dl < dh ? lo : (dh < dl ? hi : ((lo & 1) == 0 ? lo : hi));
+    }
+    return (uint8_t)(sgn | c);
+}
+
+static uint8_t mx4_group(const float* v, int n, uint8_t* q) {
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = fabsf(v[i]);
+        if (a > amax) amax = a;
+    }
+    for (int i = 0; i < 32; ++i) q[i] = 0;
+    if (amax == 0.0f) return 0;
+    int e;
+    frexp((double)amax, &e); /* floor(log2(amax)) = e - 1 */
+    int X = e - 1 - 2;
+    if (X < -127) X = -127;
+    if (X > 127) X = 127;
+    for (int i = 0; i < n; ++i) q[i] = oracle_e2m1_encode((float)ldexp((double)v[i], -X));
+    return (uint8_t)(X + 127);
+}
+
+/* MXFP4 quantisation of rows: codes [rows, Cp] (one per byte), scale bytes
+ * [rows, Cp/32], Cp = cols padded to a multiple of 128. */
+void oracle_mx4_quant_rows_f32(const float* x, int rows, int cols, uint8_t* q, uint8_t* s) {
+    int Cp = (cols + 127) / 128 * 128;
+    for (int r = 0; r < rows; ++r)
+        for (int g = 0; g < Cp / 32; ++g) {
+            int c0 = g * 32;
+            int n = cols - c0 < 32 ? (cols - c0 > 0 ? cols - c0 : 0) : 32;
+            s[(size_t)r * (Cp / 32) + g] = mx4_group(x + (size_t)r * cols + c0, n, q + (size_t)r * Cp + c0);
+        }
+}
+
+static void mx4_pack(const float* w, int rows, int cols, int rows_p, int cols_p, const int* row_map, uint8_t* q,
+                     uint8_t* s) {
+    memset(q, 0, (size_t)rows_p * cols_p);
+    memset(s, 0, (size_t)rows_p * (cols_p / 32));
+    for (int r = 0; r < rows; ++r) {
+        int d = row_map ? row_map[r] : r;
+        oracle_mx4_quant_rows_f32(w + (size_t)r * cols, 1, cols, q + (size_t)d * cols_p, s + (size_t)d * (cols_p / 32));
+    }
+}
+
+/* Weights in MXFP4: w13 [n_exp, 2I, H] -> codes [n_exp, 2Ip, Hp], scale
+ * bytes [n_exp, 2Ip, Hp/32] (gate rows [0,I), up rows [Ip, Ip+I)); w2
+ * [n_exp, H, I] -> codes [n_exp, Hp, Ip], bytes [n_exp, Hp, Ip/32]. */
+void oracle_mx4_pack_w13(const float* w13, int H, int I, int n_exp, uint8_t* q, uint8_t* s) {
+    int Hp = (H + 127) / 128 * 128, Ip = (I + 127) / 128 * 128;
+    int* map = (int*)malloc(sizeof(int) * 2 * (size_t)I);
+    for (int r = 0; r < I; ++r) {
+        map[r] = r;
+        map[I + r] = Ip + r;
+    }
+    for (int e = 0; e < n_exp; ++e)
+        mx4_pack(w13 + (size_t)e * 2 * I * H, 2 * I, H, 2 * Ip, Hp, map, q + (size_t)e * 2 * Ip * Hp,
+                 s + (size_t)e * 2 * Ip * (Hp / 32));
+    free(map);
+}
+
+void oracle_mx4_pack_w2(const float* w2, int H, int I, int n_exp, uint8_t* q, uint8_t* s) {
+    int Hp = (H + 127) / 128 * 128, Ip = (I + 127) / 128 * 128;
+    for (int e = 0; e < n_exp; ++e)
+        mx4_pack(w2 + (size_t)e * H * I, H, I, Hp, Ip, NULL, q + (size_t)e * Hp * Ip, s + (size_t)e * Hp * (Ip / 32));
+}
+
+/* The layer with MXFP4 weights (codes one per byte) and MXFP8 activations;
+ * arguments as oracle_mx_forward. */
+void oracle_mx4_forward(const uint16_t* x, const uint16_t* rw, const uint16_t* rb, const uint8_t* w13,
+                        const uint8_t* s13, const uint16_t* b13, const uint8_t* w2, const uint8_t* s2,
+                        const uint16_t* b2, int T, int H, int I, int E, int k, const int32_t* tokens, int ntok,
+                        uint16_t* out_rows, uint8_t* hq_rows, uint8_t* sh_rows, double* y_rows, int32_t* idx_rows) {
+    e4m3_init();
+    e2m1_init();
+    mx_forward_impl(x, rw, rb, w13, s13, b13, w2, s2, b2, T, H, I, E, k, tokens, ntok, out_rows, hq_rows, sh_rows,
+                    y_rows, idx_rows, E2M1);
 }
