@@ -9,11 +9,12 @@ and the step is timed with CUDA events on the launching stream; the flush is
 outside the events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
-                  [--format block128|mx]
+                  [--format block128|mx|mxfp4]
 
 --format mx runs the MXFP8 variant (1x32 UE8M0 scales on both operands,
-block-scaled tensor-core MMA) on the same workload; the default is the layer
-with 128x128 weight / 1x128 activation block scales.
+block-scaled tensor-core MMA) on the same workload; --format mxfp4 the same
+with MXFP4 weights (E2M1 codes, two per byte) and MXFP8 activations; the
+default is the layer with 128x128 weight / 1x128 activation block scales.
 
 Multi-GPU: one process per GPU (torchrun), each an independent replica of the
 same workload (the layer has no exchange step on one GPU): weak scaling,
@@ -40,7 +41,9 @@ import synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/s on 1 GB300; % of HBM (decode) / FP8 TC peak (prefill)"
 WEIGHTS = {"block128": "FP8 e4m3 128x128 block scales (x, h: 1x128), packed on device by moe_pack_weights",
-           "mx": "MXFP8: e4m3 with 1x32 UE8M0 scales on weights, x and h, packed on device by moe_pack_weights_mx"}
+           "mx": "MXFP8: e4m3 with 1x32 UE8M0 scales on weights, x and h, packed on device by moe_pack_weights_mx",
+           "mxfp4": "MXFP4 weights (E2M1, two per byte, 1x32 UE8M0 scales; packed on device by "
+                    "moe_pack_weights_mxfp4) x MXFP8 activations (x, h)"}
 DEFAULT_CONFIG = "oss20b_decode"
 FLUSH_BYTES = 256 << 20
 
@@ -60,18 +63,20 @@ def workload_str(cfg) -> str:
             f"router_b={cfg.router_b} expert_bias={cfg.expert_bias}")
 
 
-def algorithmic(cfg, counts: np.ndarray, mx: bool = False) -> dict:
+def algorithmic(cfg, counts: np.ndarray, mx: bool = False, fp4: bool = False) -> dict:
     """Algorithmic bytes / FLOPs (unpadded; activated experts only).  Scales:
     fp32 per 128x128 weight block and per 1x128 activation group, or (mx) one
-    byte per 32 values of every weight row and activation row."""
+    byte per 32 values of every weight row and activation row.  Weight codes:
+    one byte each, or half a byte (fp4: MXFP4 weights)."""
     H, I, T, k, E = cfg.H, cfg.I, cfg.T, cfg.top_k, cfg.E
     R = T * k
     act = int((counts > 0).sum())
     hb, ib = -(-H // 128), -(-I // 128)
     if mx:
         hg, ig = -(-H // 32), -(-I // 32)
-        w13 = act * (2 * I * H + 2 * I * hg + 2 * 2 * I)
-        w2 = act * (H * I + H * ig + 2 * H)
+        cb = 0.5 if fp4 else 1.0  # bytes per weight code
+        w13 = int(act * (cb * 2 * I * H + 2 * I * hg + 2 * 2 * I))
+        w2 = int(act * (cb * H * I + H * ig + 2 * H))
         sxb, shb = R * hg, R * ig
     else:
         w13 = act * (2 * I * H + 4 * 2 * ib * hb + 2 * 2 * I)
@@ -172,9 +177,9 @@ def one_per_expert_inputs(cfg):
     return x, rw, np.zeros(cfg.E, np.uint16)
 
 
-def build_layer(cfg, device, routing="synthetic", mx=False):
+def build_layer(cfg, device, routing="synthetic", mx=False, fp4=False):
     """Inputs of the workload resident on the device; weights packed by the library
-    (mx: MXFP8 codes and scale atoms)."""
+    (mx: MXFP8 codes and scale atoms; fp4: MXFP4 weight codes and scale atoms)."""
     import torch
     import sparse_moe_layer_gb300 as moe
 
@@ -188,15 +193,16 @@ def build_layer(cfg, device, routing="synthetic", mx=False):
         rw, rb = synth.router(cfg)
     b13, b2 = synth.expert_biases(cfg)
     E, H, I, Hp, Ip = cfg.E, cfg.H, cfg.I, cfg.Hp, cfg.Ip
-    w13 = torch.empty(moe.w13_shape(E, H, I), dtype=torch.uint8, device=device)
-    w2 = torch.empty(moe.w2_shape(E, H, I), dtype=torch.uint8, device=device)
-    if mx:
+    q13_shape, q2_shape = (moe.w13_shape_fp4, moe.w2_shape_fp4) if fp4 else (moe.w13_shape, moe.w2_shape)
+    w13 = torch.empty(q13_shape(E, H, I), dtype=torch.uint8, device=device)
+    w2 = torch.empty(q2_shape(E, H, I), dtype=torch.uint8, device=device)
+    if mx or fp4:
         s13 = torch.empty(moe.s13_mx_shape(E, H, I), dtype=torch.uint8, device=device)
         s2 = torch.empty(moe.s2_mx_shape(E, H, I), dtype=torch.uint8, device=device)
     else:
         s13 = torch.empty((E, 2 * Ip // 128, Hp // 128), dtype=torch.float32, device=device)
         s2 = torch.empty((E, Hp // 128, Ip // 128), dtype=torch.float32, device=device)
-    pack = moe.pack_weights_into_mx if mx else moe.pack_weights_into
+    pack = moe.pack_weights_into_mxfp4 if fp4 else moe.pack_weights_into_mx if mx else moe.pack_weights_into
     chunk = 8
     for e0 in range(0, E, chunk):
         n = min(chunk, E - e0)
@@ -209,14 +215,15 @@ def build_layer(cfg, device, routing="synthetic", mx=False):
     return layer, bf16(x), x
 
 
-def oracle_format(cfg, mx: bool):
+def oracle_format(cfg, mx: bool, fp4: bool = False):
     """Empty oracle weight arrays of the format, its per-expert packer and its layer forward."""
     import oracle
     E, Hp, Ip = cfg.E, cfg.Hp, cfg.Ip
-    if mx:
+    if mx or fp4:
         arrs = (np.zeros((E, 2 * Ip, Hp), np.uint8), np.zeros((E, 2 * Ip, Hp // 32), np.uint8),
                 np.zeros((E, Hp, Ip), np.uint8), np.zeros((E, Hp, Ip // 32), np.uint8))
-        p13, p2, fwd = oracle.mx_pack_w13, oracle.mx_pack_w2, oracle.mx_forward
+        p13, p2, fwd = ((oracle.mx4_pack_w13, oracle.mx4_pack_w2, oracle.mx4_forward) if fp4 else
+                        (oracle.mx_pack_w13, oracle.mx_pack_w2, oracle.mx_forward))
     else:
         arrs = (np.zeros((E, 2 * Ip, Hp), np.uint8), np.ones((E, 2 * Ip // 128, Hp // 128), np.float32),
                 np.zeros((E, Hp, Ip), np.uint8), np.ones((E, Hp // 128, Ip // 128), np.float32))
@@ -230,7 +237,7 @@ def oracle_format(cfg, mx: bool):
     return arrs, pack, fwd
 
 
-def cpu_oracle_leg(cfg, seconds: float, mx: bool = False):
+def cpu_oracle_leg(cfg, seconds: float, mx: bool = False, fp4: bool = False):
     """Time the oracle (single thread) on a bounded sample of the workload:
     about `seconds` of CPU work -- the tokens of a fixed random sample (at most
     the whole batch), the full layer per token, repeated if one pass is short.
@@ -241,7 +248,7 @@ def cpu_oracle_leg(cfg, seconds: float, mx: bool = False):
     b13, b2 = synth.expert_biases(cfg)
     k = cfg.top_k
     order = np.random.default_rng(1234).permutation(cfg.T).astype(np.int32)
-    (q13, s13, q2, s2), pack, fwd = oracle_format(cfg, mx)
+    (q13, s13, q2, s2), pack, fwd = oracle_format(cfg, mx, fp4)
     packed = set()
     from concurrent.futures import ThreadPoolExecutor
 
@@ -267,7 +274,7 @@ def cpu_oracle_leg(cfg, seconds: float, mx: bool = False):
         fwd(x, rw, rb, q13, s13, b13, q2, s2, b2, k, tokens=tokens)
     dt = time.perf_counter() - t0
     desc = (f"{n} of {cfg.T} tokens x {passes} pass(es) ({len(packed)} experts), full layer per token, "
-            f"single-threaded fp64 oracle" + (" (MXFP8 variant)" if mx else ""))
+            f"single-threaded fp64 oracle" + (" (MXFP4-weight variant)" if fp4 else " (MXFP8 variant)" if mx else ""))
     return passes * n / dt, desc, dt
 
 
@@ -283,8 +290,8 @@ def run_reference(args, cfg, rank):
     rng = np.random.default_rng(99)
     tokens_all = rng.permutation(cfg.T).astype(np.int32)
     r = oracle.router(np.ascontiguousarray(x[tokens_all]), rw, rb, k)
-    mx = args.format == "mx"
-    (q13, s13, q2, s2), pack, fwd = oracle_format(cfg, mx)
+    mx, fp4 = args.format == "mx", args.format == "mxfp4"
+    (q13, s13, q2, s2), pack, fwd = oracle_format(cfg, mx, fp4)
     from concurrent.futures import ThreadPoolExecutor
     needed = np.unique(r["idx"])
     with ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
@@ -319,8 +326,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=[c.name for c in synth.CONFIGS])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--format", default="block128", choices=["block128", "mx"],
-                    help="mx: the MXFP8 variant (moe_forward_mx)")
+    ap.add_argument("--format", default="block128", choices=["block128", "mx", "mxfp4"],
+                    help="mx: the MXFP8 variant (moe_forward_mx); mxfp4: MXFP4 weights (moe_forward_mxfp4)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work in the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
@@ -357,8 +364,9 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    mx = args.format == "mx"
-    layer, x_dev, x_host_np = build_layer(cfg, dev, args.routing, mx)
+    fp4 = args.format == "mxfp4"
+    mx = args.format == "mx" or fp4
+    layer, x_dev, x_host_np = build_layer(cfg, dev, args.routing, mx, fp4)
     T, H = cfg.T, cfg.H
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -371,7 +379,7 @@ def main():
     ws = layer.workspace(T)
     assert moe.read_device_status(ws) == 0, "device wait timed out during warm-up"
     counts = moe.workspace_views(ws, T, cfg.H, cfg.I, cfg.E, cfg.top_k, mx=mx)["count"].cpu().numpy()
-    alg = algorithmic(cfg, counts, mx)
+    alg = algorithmic(cfg, counts, mx, fp4)
 
     K = args.steps
     # Timed region 1 (the value): the step replayed as a CUDA graph (one memset
@@ -471,8 +479,14 @@ def main():
     else:
         roof = dict(bound="hbm", achieved=alg["gemm1_bytes"] / g1_s / 1e9, peak=pk["hbm"], unit="GB/s")
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = recorded_traffic("gemm_gateup_mx" if mx else "gemm_gateup", cfg.name, mx)
-    if mx:
+    roof["traffic"] = recorded_traffic("gemm_gateup_mx4" if fp4 else "gemm_gateup_mx" if mx else "gemm_gateup",
+                                       cfg.name, mx)
+    if fp4:
+        roof["kernel"] = ("moe_gemm_mx_kernel<true, FP4W> (block-scaled e4m3 x e2m1 gate/up GEMM + SwiGLU + MX "
+                          "requant)" if prefill else
+                          "moe_gemm_mx_decode_kernel<true, FP4W> (swap-AB block-scaled e2m1 x e4m3 gate/up GEMM + "
+                          "SwiGLU + MX requant)")
+    elif mx:
         roof["kernel"] = ("moe_gemm_mx_kernel<true> (block-scaled gate/up GEMM + SwiGLU + MX requant)" if prefill else
                           "moe_gemm_mx_decode_kernel<true> (swap-AB block-scaled gate/up GEMM + SwiGLU + MX requant)")
     else:
@@ -483,7 +497,8 @@ def main():
 
     value = world * T / (ms * 1e-3)
     line = dict(metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=K, warmup=args.warmup,
-                ms_per_step=ms, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="e4m3",
+                ms_per_step=ms, higher_is_better=True, scaling="weak", vs_baseline=None,
+                dtype="e2m1 x e4m3" if fp4 else "e4m3",
                 data="synthetic",
                 config=dict(workload=workload_str(cfg) + ("" if args.routing == "synthetic" else
                                                           " routing=one row per expert (T = E/top_k)"),
@@ -498,14 +513,15 @@ def main():
                           step_hbm_frac=alg["step_bytes"] / (ms * 1e-3) / 1e9 / pk["hbm"],
                           gemm_tflops=(alg["gemm1_flops"] + alg["gemm2_flops"]) / (ms * 1e-3) / 1e12,
                           wall_s=wall, device_status=status,
-                          launch="CUDA graph replay of " + ("moe_forward_mx" if mx else "moe_forward"),
+                          launch="CUDA graph replay of " + ("moe_forward_mxfp4" if fp4 else "moe_forward_mx" if mx
+                                                            else "moe_forward"),
                           eager_ms_per_step=eager_ms),
                 e2e=dict(value=world * T / (e2e_ms * 1e-3), unit="tokens/s", h2d_bytes_per_step=T * H * 2,
                          d2h_bytes_per_step=T * H * 2, ms_per_step=e2e_ms),
                 gpu_launches=5 * K,
                 clocks=sampler.summary())
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, desc, dt = cpu_oracle_leg(cfg, args.cpu_seconds, mx)
+        v, desc, dt = cpu_oracle_leg(cfg, args.cpu_seconds, mx, fp4)
         line["cpu_baseline"] = dict(value=v, unit="tokens/s", cores=1, kind="oracle", sample=desc, seconds=dt)
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -228,6 +228,47 @@ moe_status moe_pack_weights_mx(const float* w13_f32, const float* w2_f32, int H,
 moe_status moe_quantize_rows_mx(const float* in, int rows, int cols, int ld_in, uint8_t* q, uint8_t* s,
                                 void* stream);
 
+/* ---------------------------------------------------------------------------
+ * MXFP4 weights.  "GPT-OSS on Day 0" (opening section): the open-weight
+ * models ship with MXFP4 weights, which Blackwell's FP4 tensor cores run
+ * natively; "Hosting Qwen on Blackwell" (section "Quantization") names the
+ * microscaled formats as the fast path there.  Weights are OCP MX v1.0 FP4
+ * E2M1 codes (section 5.3.3: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6, sign in
+ * bit 3) with one UE8M0 scale per 32 values along K, shared exponent
+ * floor(log2(amax)) - 2 (section 6.3); x and h stay MXFP8 exactly as in
+ * moe_forward_mx.  The codes are packed two per byte, value 2j in the low
+ * nibble of byte j, each 128 x 128 block contiguous (64-byte rows):
+ *   w13 uint8 [E, 2*Ip/128, Hp/128, 128, 64]   w2 uint8 [E, Hp/128, Ip/128, 128, 64]
+ * the scale atoms are those of the MXFP8 layout.  Half the weight bytes of
+ * the e4m3 formats.
+ * ------------------------------------------------------------------------- */
+
+/*
+ * The layer with MXFP4 weights.  Arguments as moe_forward_mx, with w13 and w2
+ * in the packed layout above (device, 32-byte aligned, else
+ * MOE_ERR_UNSUPPORTED).  The workspace is sized by moe_workspace_size_mx.
+ */
+moe_status moe_forward_mxfp4(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
+                             const uint8_t* s13, const void* b13, const uint8_t* w2, const uint8_t* s2, const void* b2,
+                             int T, int H, int I, int E, int top_k, void* out, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* moe_forward_mxfp4 with the timing marks of moe_forward_profiled. */
+moe_status moe_forward_mxfp4_profiled(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
+                                      const uint8_t* s13, const void* b13, const uint8_t* w2, const uint8_t* s2,
+                                      const void* b2, int T, int H, int I, int E, int top_k, void* out,
+                                      void* workspace, size_t workspace_bytes, void* stream, void* const* events);
+
+/*
+ * MXFP4 weight packer: fp32 masters (as moe_pack_weights) -> packed E2M1
+ * codes (nearest, ties to the even code, magnitudes above 6 * 2^X saturate)
+ * and scale atoms.  An all-zero group gets byte 0 and +0 codes; padding rows
+ * and columns are zero.  Output pointers 16-byte aligned (32 for use by
+ * moe_forward_mxfp4); either input may be NULL.
+ */
+moe_status moe_pack_weights_mxfp4(const float* w13_f32, const float* w2_f32, int H, int I, int E, uint8_t* w13,
+                                  uint8_t* s13, uint8_t* w2, uint8_t* s2, void* stream);
+
 /* Synchronises `stream`, then reads and clears the device error word of
  * `workspace`: MOE_OK, MOE_ERR_DEVICE_TIMEOUT (a bounded wait ran out), or
  * MOE_ERR_CUDA. */

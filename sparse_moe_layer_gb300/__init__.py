@@ -18,7 +18,9 @@ from .build import LIB, build
 __all__ = ["MoeError", "build", "lib", "workspace_size", "workspace_layout", "workspace_views", "forward",
            "pack_weights", "pack_weights_into", "w13_shape", "w2_shape", "unblock", "quantize_rows",
            "read_device_status", "test_bounded_wait", "MoeLayer", "pad128", "pack_weights_mx",
-           "pack_weights_into_mx", "s13_mx_shape", "s2_mx_shape", "unblock_scales_mx", "quantize_rows_mx"]
+           "pack_weights_into_mx", "s13_mx_shape", "s2_mx_shape", "unblock_scales_mx", "quantize_rows_mx",
+           "pack_weights_mxfp4", "pack_weights_into_mxfp4", "w13_shape_fp4", "w2_shape_fp4", "unblock_fp4",
+           "weight_format"]
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "CUDA error",
           5: "device wait timed out"}
@@ -75,6 +77,12 @@ def lib():
         L.moe_pack_weights_mx.restype = i32
         L.moe_quantize_rows_mx.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         L.moe_quantize_rows_mx.restype = i32
+        L.moe_forward_mxfp4.argtypes = [vp] * 9 + [i32] * 5 + [vp, vp, sz, vp]
+        L.moe_forward_mxfp4.restype = i32
+        L.moe_forward_mxfp4_profiled.argtypes = [vp] * 9 + [i32] * 5 + [vp, vp, sz, vp, vp]
+        L.moe_forward_mxfp4_profiled.restype = i32
+        L.moe_pack_weights_mxfp4.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+        L.moe_pack_weights_mxfp4.restype = i32
         L.moe_read_device_status.argtypes = [vp, vp]
         L.moe_read_device_status.restype = i32
         L.moe_test_bounded_wait.argtypes = [u64, i32, vp, vp]
@@ -172,21 +180,33 @@ def workspace_views(ws: torch.Tensor, T: int, H: int, I: int, E: int, top_k: int
 STAGES = ("router", "permute_quant", "gemm_gateup", "gemm_down", "combine")
 
 
+def weight_format(w13: torch.Tensor, s13: torch.Tensor) -> str:
+    """"block128" (fp32 block scales), "mxfp8" (uint8 scale atoms, e4m3 codes) or
+    "mxfp4" (uint8 scale atoms, E2M1 codes two per byte: 64-byte block rows)."""
+    if s13.dtype != torch.uint8:
+        return "block128"
+    return "mxfp4" if w13.shape[-1] == 64 else "mxfp8"
+
+
 def forward(x, router_w, router_b, w13, s13, b13, w2, s2, b2, top_k: int, out=None, workspace=None, stream=None,
             events=None):
     """out [T, H] bf16 = the MoE layer applied to x [T, H] bf16.
 
-    Weights from pack_weights (fp32 128x128 block scales: moe_forward) or from
-    pack_weights_mx (uint8 MX scale atoms: moe_forward_mx); the scales' dtype
-    selects the variant.  events: optional list of 6
+    Weights from pack_weights (fp32 128x128 block scales: moe_forward), from
+    pack_weights_mx (uint8 MX scale atoms: moe_forward_mx) or from
+    pack_weights_mxfp4 (packed E2M1 codes: moe_forward_mxfp4); weight_format()
+    tells them apart.  events: optional list of 6
     torch.cuda.Event(enable_timing=True); event i is recorded before stage i
     (STAGES) and event 5 after the last stage."""
     T, H = x.shape
     E = router_w.shape[0]
     I = b13.shape[1] // 2
     Hp, Ip = pad128(H), pad128(I)
-    mx = s13.dtype == torch.uint8
-    if tuple(w13.shape) != w13_shape(E, H, I) or tuple(w2.shape) != w2_shape(E, H, I):
+    fmt = weight_format(w13, s13)
+    mx = fmt != "block128"
+    shapes = (w13_shape_fp4(E, H, I), w2_shape_fp4(E, H, I)) if fmt == "mxfp4" else (w13_shape(E, H, I),
+                                                                                     w2_shape(E, H, I))
+    if (tuple(w13.shape), tuple(w2.shape)) != shapes:
         raise ValueError(f"packed weight shapes {tuple(w13.shape)}, {tuple(w2.shape)} do not match H={H} I={I} E={E}")
     if mx:
         if tuple(s13.shape) != s13_mx_shape(E, H, I) or tuple(s2.shape) != s2_mx_shape(E, H, I):
@@ -205,14 +225,15 @@ def forward(x, router_w, router_b, w13, s13, b13, w2, s2, b2, top_k: int, out=No
     tail = (_dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
             _stream(stream))
     L = lib()
+    name = {"block128": "moe_forward", "mxfp8": "moe_forward_mx", "mxfp4": "moe_forward_mxfp4"}[fmt]
     if events is None:
-        code = (L.moe_forward_mx if mx else L.moe_forward)(*ptrs, T, H, I, E, top_k, *tail)
+        code = getattr(L, name)(*ptrs, T, H, I, E, top_k, *tail)
     else:
         if len(events) != 6:
             raise ValueError("events must hold 6 CUDA events")
         arr = (ctypes.c_void_p * 6)(*[ev.cuda_event for ev in events])
-        code = (L.moe_forward_mx_profiled if mx else L.moe_forward_profiled)(*ptrs, T, H, I, E, top_k, *tail, arr)
-    _check(code, "moe_forward_mx" if mx else "moe_forward")
+        code = getattr(L, name + "_profiled")(*ptrs, T, H, I, E, top_k, *tail, arr)
+    _check(code, name)
     return out
 
 
@@ -307,6 +328,49 @@ def pack_weights_into_mx(w13_f32, w2_f32, H: int, I: int, E: int, q13, s13, q2, 
     _check(code, "moe_pack_weights_mx")
 
 
+def w13_shape_fp4(E: int, H: int, I: int) -> tuple:
+    """Packed MXFP4 gate/up codes: blocked [E, 2*Ip/128, Hp/128, 128, 64], two E2M1 codes per byte."""
+    return (E, 2 * pad128(I) // 128, pad128(H) // 128, 128, 64)
+
+
+def w2_shape_fp4(E: int, H: int, I: int) -> tuple:
+    """Packed MXFP4 down codes: blocked [E, Hp/128, Ip/128, 128, 64]."""
+    return (E, pad128(H) // 128, pad128(I) // 128, 128, 64)
+
+
+def unblock_fp4(q: torch.Tensor) -> torch.Tensor:
+    """Blocked packed E2M1 codes [E, RB, KB, 128, 64] -> one code per byte, row-major
+    [E, RB*128, KB*128] (value 2j of a row is the low nibble of byte j; for inspection)."""
+    codes = torch.stack((q & 15, q >> 4), dim=-1).reshape(*q.shape[:4], 128)
+    return unblock(codes)
+
+
+def pack_weights_mxfp4(w13_f32: torch.Tensor, w2_f32: torch.Tensor, stream=None):
+    """fp32 masters w13 [E, 2I, H], w2 [E, H, I] -> (w13 packed E2M1 codes, s13 atoms, w2 codes, s2 atoms)."""
+    E, twoI, H = w13_f32.shape
+    I = twoI // 2
+    dev = w13_f32.device
+    if tuple(w2_f32.shape) != (E, H, I):
+        raise ValueError("w2 shape does not match w13")
+    out = (torch.empty(w13_shape_fp4(E, H, I), dtype=torch.uint8, device=dev),
+           torch.empty(s13_mx_shape(E, H, I), dtype=torch.uint8, device=dev),
+           torch.empty(w2_shape_fp4(E, H, I), dtype=torch.uint8, device=dev),
+           torch.empty(s2_mx_shape(E, H, I), dtype=torch.uint8, device=dev))
+    pack_weights_into_mxfp4(w13_f32, w2_f32, H, I, E, *out, stream=stream)
+    return out
+
+
+def pack_weights_into_mxfp4(w13_f32, w2_f32, H: int, I: int, E: int, q13, s13, q2, s2, stream=None):
+    """MXFP4-pack a slice of experts (either master may be None) into preallocated outputs."""
+    code = lib().moe_pack_weights_mxfp4(None if w13_f32 is None else _dev(w13_f32, torch.float32, "w13_f32"),
+                                        None if w2_f32 is None else _dev(w2_f32, torch.float32, "w2_f32"), H, I, E,
+                                        None if q13 is None else _dev(q13, torch.uint8, "w13"),
+                                        None if s13 is None else _dev(s13, torch.uint8, "s13"),
+                                        None if q2 is None else _dev(q2, torch.uint8, "w2"),
+                                        None if s2 is None else _dev(s2, torch.uint8, "s2"), _stream(stream))
+    _check(code, "moe_pack_weights_mxfp4")
+
+
 def quantize_rows_mx(v: torch.Tensor, stream=None):
     """1x32 MX quantisation of fp32 rows [rows, cols] -> (codes [rows, cols_p] u8, UE8M0 bytes [rows, cols_p/32])."""
     rows, cols = v.shape
@@ -352,7 +416,7 @@ class MoeLayer:
         self.top_k = top_k
         self.E, self.H = router_w.shape
         self.I = b13.shape[1] // 2
-        self.mx = s13.dtype == torch.uint8  # MXFP8 scale atoms (pack_weights_mx)
+        self.mx = s13.dtype == torch.uint8  # MX scale atoms (pack_weights_mx / pack_weights_mxfp4)
         self._ws = None
 
     def workspace(self, T: int) -> torch.Tensor:

@@ -95,6 +95,24 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
     return r == CUDA_SUCCESS;
 }
 
+// Blocked MXFP4 weight codes as a 2D tensor of 4-bit values [rows, 128], two
+// per byte (64-byte rows), box 128 values x 128 rows, 128-byte swizzle.  The
+// 16U4_ALIGN16B type lands each 16-value chunk in 16 bytes of shared memory
+// (8 bytes of codes, 8 bytes of gap): the padded form the f8f6f4 MMA kinds
+// read.  The type needs a 32-byte aligned base.
+bool make_map_fp4(CUtensorMap* m, const void* base, uint64_t rows) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {64};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int num_sms() {
     int dev = 0, n = 0;
     cudaGetDevice(&dev);
@@ -103,17 +121,22 @@ int num_sms() {
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
+// Weight formats of forward_impl.
+enum WeightFormat { kBlock128 = 0, kMxfp8 = 1, kMxfp4 = 2 };
 
 }  // namespace
 
 // Launch sequence shared by moe_forward and moe_forward_profiled; when `ev`
 // is non-null, ev[i] is recorded on the stream before stage i and ev[5]
 // after the last stage.
-// mx: the MXFP8 variant (s13, s2 are UE8M0 scale atoms, not fp32 block scales).
+// fmt: kBlock128 (e4m3 codes, fp32 128x128 block scales), kMxfp8 (e4m3 codes,
+// UE8M0 scale atoms) or kMxfp4 (E2M1 codes two per byte, UE8M0 scale atoms).
 static moe_status forward_impl(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
                                const void* s13, const void* b13, const uint8_t* w2, const void* s2, const void* b2,
                                int T, int H, int I, int E, int top_k, void* out, void* workspace,
-                               size_t workspace_bytes, void* stream, void* const* ev, bool mx = false);
+                               size_t workspace_bytes, void* stream, void* const* ev, int fmt = kBlock128);
 
 extern "C" {
 
@@ -166,7 +189,7 @@ moe_status moe_forward_mx(const void* x, const void* router_w, const void* route
                           int T, int H, int I, int E, int top_k, void* out, void* workspace, size_t workspace_bytes,
                           void* stream) {
     return forward_impl(x, router_w, router_b, w13, s13, b13, w2, s2, b2, T, H, I, E, top_k, out, workspace,
-                        workspace_bytes, stream, nullptr, true);
+                        workspace_bytes, stream, nullptr, kMxfp8);
 }
 
 moe_status moe_forward_mx_profiled(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
@@ -177,7 +200,26 @@ moe_status moe_forward_mx_profiled(const void* x, const void* router_w, const vo
     for (int i = 0; i < 6; ++i)
         if (!events[i]) return MOE_ERR_INVALID_ARG;
     return forward_impl(x, router_w, router_b, w13, s13, b13, w2, s2, b2, T, H, I, E, top_k, out, workspace,
-                        workspace_bytes, stream, events, true);
+                        workspace_bytes, stream, events, kMxfp8);
+}
+
+moe_status moe_forward_mxfp4(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
+                             const uint8_t* s13, const void* b13, const uint8_t* w2, const uint8_t* s2, const void* b2,
+                             int T, int H, int I, int E, int top_k, void* out, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+    return forward_impl(x, router_w, router_b, w13, s13, b13, w2, s2, b2, T, H, I, E, top_k, out, workspace,
+                        workspace_bytes, stream, nullptr, kMxfp4);
+}
+
+moe_status moe_forward_mxfp4_profiled(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
+                                      const uint8_t* s13, const void* b13, const uint8_t* w2, const uint8_t* s2,
+                                      const void* b2, int T, int H, int I, int E, int top_k, void* out,
+                                      void* workspace, size_t workspace_bytes, void* stream, void* const* events) {
+    if (!events) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 6; ++i)
+        if (!events[i]) return MOE_ERR_INVALID_ARG;
+    return forward_impl(x, router_w, router_b, w13, s13, b13, w2, s2, b2, T, H, I, E, top_k, out, workspace,
+                        workspace_bytes, stream, events, kMxfp4);
 }
 
 }  // extern "C"
@@ -185,7 +227,8 @@ moe_status moe_forward_mx_profiled(const void* x, const void* router_w, const vo
 static moe_status forward_impl(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
                                const void* s13, const void* b13, const uint8_t* w2, const void* s2, const void* b2,
                                int T, int H, int I, int E, int top_k, void* out, void* workspace,
-                               size_t workspace_bytes, void* stream, void* const* ev, bool mx) {
+                               size_t workspace_bytes, void* stream, void* const* ev, int fmt) {
+    const bool mx = fmt != kBlock128;
     auto mark = [&](int i) {
         if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), static_cast<cudaStream_t>(stream));
     };
@@ -196,6 +239,7 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return MOE_ERR_UNSUPPORTED;
     if (mx && (!aligned16(s13) || !aligned16(s2))) return MOE_ERR_UNSUPPORTED;  // scale atoms move by bulk copy
+    if (fmt == kMxfp4 && (!aligned32(w13) || !aligned32(w2))) return MOE_ERR_UNSUPPORTED;  // 4-bit tensor maps
     moe_workspace_layout L;
     layout_of(T, H, I, E, top_k, &L, mx);
     if (workspace_bytes < L.total_bytes) return MOE_ERR_WORKSPACE;
@@ -281,8 +325,10 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     // weights are blocked: a 2D view of 128-byte rows, one 128x128 block = 128 consecutive rows
     // decode kernels load a tile's activation rows in boxes of kDecXBoxRows, only as many as it has rows
     const uint32_t a_box = decode ? kDecXBoxRows : (uint32_t)rp.bm;
-    if (!make_map(&tmA1, pp.xq, R, Hp, a_box) || !make_map(&tmB1, w13, (uint64_t)E * 2 * Ip * (Hp / 128), 128) ||
-        !make_map(&tmA2, ws + L.hq, R, Ip, a_box) || !make_map(&tmB2, w2, (uint64_t)E * Hp * (Ip / 128), 128))
+    const uint64_t rows13 = (uint64_t)E * 2 * Ip * (Hp / 128), rows2 = (uint64_t)E * Hp * (Ip / 128);
+    const bool wmaps = fmt == kMxfp4 ? make_map_fp4(&tmB1, w13, rows13) && make_map_fp4(&tmB2, w2, rows2)
+                                     : make_map(&tmB1, w13, rows13, 128) && make_map(&tmB2, w2, rows2, 128);
+    if (!wmaps || !make_map(&tmA1, pp.xq, R, Hp, a_box) || !make_map(&tmA2, ws + L.hq, R, Ip, a_box))
         return MOE_ERR_CUDA;
 
     if (mx) {
@@ -306,7 +352,7 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
         m1.ldq = Ip;
         m1.status = rp.status;
         const long long t1 = mt_bound * rp.nt1;
-        if (launch_gemm_mx(true, decode, tmA1, tmB1, m1, (int)(t1 < sms ? t1 : sms), st) != cudaSuccess)
+        if (launch_gemm_mx(true, decode, fmt == kMxfp4, tmA1, tmB1, m1, (int)(t1 < sms ? t1 : sms), st) != cudaSuccess)
             return MOE_ERR_CUDA;
         mark(3);
         MxGemmParams m2;
@@ -329,7 +375,7 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
         m2.ldp = Hp;
         m2.status = rp.status;
         const long long t2 = mt_bound * rp.nt2;
-        if (launch_gemm_mx(false, decode, tmA2, tmB2, m2, (int)(t2 < sms ? t2 : sms), st) != cudaSuccess)
+        if (launch_gemm_mx(false, decode, fmt == kMxfp4, tmA2, tmB2, m2, (int)(t2 < sms ? t2 : sms), st) != cudaSuccess)
             return MOE_ERR_CUDA;
         mark(4);
         if (launch_combine(m2.part, T, H, Hp, top_k, static_cast<uint16_t*>(out), sms, st) != cudaSuccess)
@@ -473,6 +519,21 @@ moe_status moe_pack_weights_mx(const float* w13_f32, const float* w2_f32, int H,
     if (w13_f32 && launch_pack_blocks_mx(w13_f32, E, 2 * I, H, 2 * Ip, Hp, I, w13, s13, st) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (w2_f32 && launch_pack_blocks_mx(w2_f32, E, H, I, Hp, Ip, 0, w2, s2, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status moe_pack_weights_mxfp4(const float* w13_f32, const float* w2_f32, int H, int I, int E, uint8_t* w13,
+                                  uint8_t* s13, uint8_t* w2, uint8_t* s2, void* stream) {
+    if (H < 1 || I < 1 || E < 1 || H > 16384 || I > 16384 || E > kMaxExperts) return MOE_ERR_INVALID_ARG;
+    if (!w13_f32 && !w2_f32) return MOE_ERR_INVALID_ARG;
+    if ((w13_f32 && (!w13 || !s13)) || (w2_f32 && (!w2 || !s2))) return MOE_ERR_INVALID_ARG;
+    if ((w13 && !aligned16(w13)) || (w2 && !aligned16(w2)) || (s13 && !aligned16(s13)) || (s2 && !aligned16(s2)))
+        return MOE_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int Hp = pad128(H), Ip = pad128(I);
+    if (w13_f32 && launch_pack_blocks_mx4(w13_f32, E, 2 * I, H, 2 * Ip, Hp, I, w13, s13, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (w2_f32 && launch_pack_blocks_mx4(w2_f32, E, H, I, Hp, Ip, 0, w2, s2, st) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
 }
 

@@ -329,6 +329,14 @@ __device__ __forceinline__ void mma_e4m3(uint32_t tmem_d, uint64_t adesc, uint64
 __host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N) {
     return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
 }
+// Operand format codes of the f8f6f4 kinds (A: bits 7-9, B: bits 10-12):
+// e4m3 = 0, e2m1 (FP4) = 5.  An e2m1 operand sits in shared memory in the
+// padded form: each 16-byte chunk holds 16 packed 4-bit values in its first 8
+// bytes, so a 128-value K block still spans one 128-byte row.
+constexpr uint32_t kFmtE4M3 = 0, kFmtE2M1 = 5;
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t afmt, uint32_t bfmt) {
+    return idesc_mx_e4m3(M, N) | (afmt << 7) | (bfmt << 10);
+}
 // ... with the byte of the scale cells this MMA reads (B: bits 4-5, A: bits 29-30).
 __device__ __forceinline__ uint32_t idesc_sf_id(uint32_t idesc, uint32_t id) { return idesc | (id << 4) | (id << 29); }
 

@@ -29,6 +29,18 @@
 //   down:    * routing weight -> part[t*k+j, :].
 // Every mbarrier wait is bounded; a timeout sets an error bit and all roles
 // drain and exit.
+//
+// MXFP4 weights (FP4W): "GPT-OSS on Day 0" (opening section) notes that the
+// open-weight models ship with MXFP4 weights and that Blackwell's FP4 tensor
+// cores run them natively.  The weight codes are E2M1, two per byte in HBM
+// (half the bytes of the e4m3 codes, which is what decode-sized batches are
+// bound by); the tensor map's 16U4_ALIGN16B type expands each 16-value chunk
+// into the 16-byte padded form the f8f6f4 MMA kinds read, so the shared-memory
+// image, the stage ring, the scale atoms and the descriptors are those of the
+// e4m3 weights; what changes is the instruction descriptor's weight format and
+// the byte count a weight box completes on its stage barrier (the packed
+// global bytes, 8 KB per 128 x 128 box, not the 16 KB it fills).
+// Activations stay MXFP8 (e4m3 codes).
 #include <cuda_bf16.h>
 
 #include "moe_device.cuh"
@@ -63,13 +75,16 @@ __device__ __forceinline__ MxTile mx_tile(int tile, const int* s_tiles, const in
 }
 
 // ===================================================================== prefill
-template <bool GATED>
+template <bool GATED, bool FP4W>
 struct MxCfg {
     static constexpr int BM = 128;
     static constexpr int BN = 256;
     static constexpr int A_BYTES = BM * 128;
     static constexpr int B_BYTES = BN * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    // bytes a stage's loads complete on its barrier: a 4-bit weight box counts its
+    // packed global bytes (half its shared-memory footprint)
+    static constexpr int STAGE_TX = A_BYTES + (FP4W ? B_BYTES / 2 : B_BYTES);
     static constexpr int SF_BYTES = 3 * kMxAtomBytes;  // activation tile, weight block 0, weight block 1
     static constexpr int STAGES = 4;
     static constexpr int SF_COL0 = BN;                 // TMEM: accumulator [0, 256), scale ring after it
@@ -79,15 +94,16 @@ struct MxCfg {
     static constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter (warp & 3)
     static constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
     static constexpr int SMEM_BYTES = STAGES * (STAGE_BYTES + SF_BYTES) + 1024;
-    static constexpr uint32_t IDESC = idesc_mx_e4m3(BM, BN);
+    // A = activation codes (e4m3), B = weight codes (e4m3, or e2m1 for MXFP4 weights)
+    static constexpr uint32_t IDESC = idesc_mx(BM, BN, kFmtE4M3, FP4W ? kFmtE2M1 : kFmtE4M3);
     static_assert(SF_COL0 + STAGES * SF_STRIDE <= TMEM_COLS, "scale ring does not fit in TMEM");
 };
 
-template <bool GATED>
-__global__ void __launch_bounds__(MxCfg<GATED>::THREADS, 1)
+template <bool GATED, bool FP4W>
+__global__ void __launch_bounds__(MxCfg<GATED, FP4W>::THREADS, 1)
     moe_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                        const MxGemmParams p) {
-    using C = MxCfg<GATED>;
+    using C = MxCfg<GATED, FP4W>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sf_smem = smem + C::STAGES * C::STAGE_BYTES;
@@ -174,7 +190,7 @@ __global__ void __launch_bounds__(MxCfg<GATED>::THREADS, 1)
                         break;
                     }
                     const uint32_t fb = smem_u32(&full_bar[stage]);
-                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES + C::SF_BYTES);
+                    mbar_arrive_expect_tx(fb, C::STAGE_TX + C::SF_BYTES);
                     const uint32_t a_dst = smem_u32(smem + stage * C::STAGE_BYTES);
                     const uint32_t b_dst = a_dst + C::A_BYTES;
                     const uint32_t sf_dst = smem_u32(sf_smem + stage * C::SF_BYTES);
@@ -394,12 +410,13 @@ __global__ void __launch_bounds__(MxCfg<GATED>::THREADS, 1)
 }
 
 // ====================================================================== decode
-template <bool GATED>
+template <bool GATED, bool FP4W>
 struct MxDecCfg {
     static constexpr int BT = 32;  // token rows per tile (MMA N)
     static constexpr int W_BYTES = (GATED ? 2 : 1) * 128 * 128;
     static constexpr int X_BYTES = BT * 128;
     static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
+    static constexpr int W_TX = FP4W ? W_BYTES / 2 : W_BYTES;  // packed bytes of 4-bit weight boxes
     static constexpr int SF_BYTES = (GATED ? 3 : 2) * kMxAtomBytes;  // weight block(s), token tile
     static constexpr int MAX_STAGES = 16;
     static constexpr int ACC_COLS = GATED ? 2 * BT : BT;
@@ -410,16 +427,17 @@ struct MxDecCfg {
     static constexpr int EPI_WARPS = 4;
     static constexpr int META_WARP = 6;
     static constexpr int THREADS = 7 * 32;
-    static constexpr uint32_t IDESC = idesc_mx_e4m3(128, BT);
+    // A = weight codes (e4m3, or e2m1 for MXFP4 weights), B = token codes (e4m3)
+    static constexpr uint32_t IDESC = idesc_mx(128, BT, FP4W ? kFmtE2M1 : kFmtE4M3, kFmtE4M3);
     static_assert(NACC * ACC_COLS <= SF_COL0, "accumulators overlap the scale ring");
     static_assert(SF_COL0 + MAX_STAGES * SF_STRIDE <= TMEM_COLS, "scale ring does not fit in TMEM");
 };
 
-template <bool GATED>
-__global__ void __launch_bounds__(MxDecCfg<GATED>::THREADS, 1)
+template <bool GATED, bool FP4W>
+__global__ void __launch_bounds__(MxDecCfg<GATED, FP4W>::THREADS, 1)
     moe_gemm_mx_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                               const MxGemmParams p, const int nst) {
-    using C = MxDecCfg<GATED>;
+    using C = MxDecCfg<GATED, FP4W>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sf_smem = smem + nst * C::STAGE_BYTES;
@@ -483,11 +501,11 @@ __global__ void __launch_bounds__(MxDecCfg<GATED>::THREADS, 1)
             int stage = 0;
             uint32_t phase = 0, filled = 0;
             bool ok = true;
+            const int ublk = GATED ? (p.up_rows / 128) * p.KB : 0;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const MxTile ti = mx_tile<C::BT>(tile, s_tiles, s_off, s_cnt, E);
                 const int mtid = s_tiles[ti.e] / p.nt + ti.mt;
                 const int wblk = (ti.e * p.sw_rowblocks + ti.nt) * p.KB;
-                const int ublk = GATED ? (p.up_rows / 128) * p.KB : 0;
                 const int nxb = (ti.rows + kDecXBoxRows - 1) / kDecXBoxRows;
                 const uint8_t* sa = p.sa + (size_t)mtid * p.KB * kMxAtomBytes;
                 for (int kb = 0; kb < p.KB; ++kb) {
@@ -496,7 +514,7 @@ __global__ void __launch_bounds__(MxDecCfg<GATED>::THREADS, 1)
                         break;
                     }
                     const uint32_t fb = smem_u32(&full_bar[stage]);
-                    mbar_arrive_expect_tx(fb, C::W_BYTES + nxb * kDecXBoxRows * 128 + C::SF_BYTES);
+                    mbar_arrive_expect_tx(fb, C::W_TX + nxb * kDecXBoxRows * 128 + C::SF_BYTES);
                     const uint32_t w_dst = smem_u32(smem + stage * C::STAGE_BYTES);
                     const uint32_t sf_dst = smem_u32(sf_smem + stage * C::SF_BYTES);
                     tma_load_2d(w_dst, &tmW, 0, (wblk + kb) * 128, fb);
@@ -702,27 +720,28 @@ __global__ void __launch_bounds__(MxDecCfg<GATED>::THREADS, 1)
 }
 
 // ===================================================================== launch
-template <bool GATED>
+template <bool GATED, bool FP4W>
 static cudaError_t launch_mx_prefill(const CUtensorMap& tmX, const CUtensorMap& tmW, const MxGemmParams& p, int grid,
                                      cudaStream_t st) {
-    using C = MxCfg<GATED>;
-    cudaError_t e =
-        cudaFuncSetAttribute(moe_gemm_mx_kernel<GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    using C = MxCfg<GATED, FP4W>;
+    cudaError_t e = cudaFuncSetAttribute(moe_gemm_mx_kernel<GATED, FP4W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    return launch_pdl(moe_gemm_mx_kernel<GATED>, dim3(grid), dim3(C::THREADS), (size_t)C::SMEM_BYTES, st, tmX, tmW, p);
+    return launch_pdl(moe_gemm_mx_kernel<GATED, FP4W>, dim3(grid), dim3(C::THREADS), (size_t)C::SMEM_BYTES, st, tmX,
+                      tmW, p);
 }
 
 // The stage ring takes the shared memory the kernel's static arrays leave, up
 // to `max_stages` stages.
-template <bool GATED>
+template <bool GATED, bool FP4W>
 static cudaError_t launch_mx_decode(const CUtensorMap& tmX, const CUtensorMap& tmW, const MxGemmParams& p, int grid,
                                     int max_stages, cudaStream_t st) {
-    using C = MxDecCfg<GATED>;
+    using C = MxDecCfg<GATED, FP4W>;
     int dev = 0, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     cudaFuncAttributes fa;
-    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, moe_gemm_mx_decode_kernel<GATED>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, moe_gemm_mx_decode_kernel<GATED, FP4W>);
     if (e != cudaSuccess) return e;
     const long long room = (long long)optin - (long long)fa.sharedSizeBytes - 1024;
     int nst = (int)(room / (C::STAGE_BYTES + C::SF_BYTES));
@@ -730,17 +749,27 @@ static cudaError_t launch_mx_decode(const CUtensorMap& tmX, const CUtensorMap& t
     if (nst > C::MAX_STAGES) nst = C::MAX_STAGES;
     if (nst < 2) return cudaErrorInvalidConfiguration;
     const size_t smem = (size_t)nst * (C::STAGE_BYTES + C::SF_BYTES) + 1024;
-    e = cudaFuncSetAttribute(moe_gemm_mx_decode_kernel<GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(moe_gemm_mx_decode_kernel<GATED, FP4W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(moe_gemm_mx_decode_kernel<GATED>, dim3(grid), dim3(C::THREADS), smem, st, tmX, tmW, p, nst);
+    return launch_pdl(moe_gemm_mx_decode_kernel<GATED, FP4W>, dim3(grid), dim3(C::THREADS), smem, st, tmX, tmW, p,
+                      nst);
 }
 
-cudaError_t launch_gemm_mx(bool gated, bool decode, const CUtensorMap& tmX, const CUtensorMap& tmW,
-                           const MxGemmParams& p, int grid, cudaStream_t st) {
+template <bool FP4W>
+static cudaError_t launch_mx(bool gated, bool decode, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                             const MxGemmParams& p, int grid, cudaStream_t st) {
     if (decode)
-        return gated ? launch_mx_decode<true>(tmX, tmW, p, grid, kDecStagesGateUp, st)
-                     : launch_mx_decode<false>(tmX, tmW, p, grid, kDecStagesDown, st);
-    return gated ? launch_mx_prefill<true>(tmX, tmW, p, grid, st) : launch_mx_prefill<false>(tmX, tmW, p, grid, st);
+        return gated ? launch_mx_decode<true, FP4W>(tmX, tmW, p, grid, kDecStagesGateUp, st)
+                     : launch_mx_decode<false, FP4W>(tmX, tmW, p, grid, kDecStagesDown, st);
+    return gated ? launch_mx_prefill<true, FP4W>(tmX, tmW, p, grid, st)
+                 : launch_mx_prefill<false, FP4W>(tmX, tmW, p, grid, st);
+}
+
+cudaError_t launch_gemm_mx(bool gated, bool decode, bool fp4w, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                           const MxGemmParams& p, int grid, cudaStream_t st) {
+    return fp4w ? launch_mx<true>(gated, decode, tmX, tmW, p, grid, st)
+                : launch_mx<false>(gated, decode, tmX, tmW, p, grid, st);
 }
 
 }  // namespace moe

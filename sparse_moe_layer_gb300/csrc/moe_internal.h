@@ -142,6 +142,8 @@ cudaError_t launch_quantize_rows(const float* in, int rows, int cols, int ld_in,
                                  cudaStream_t st);
 cudaError_t launch_pack_blocks_mx(const float* src, int E, int rows_src, int cols, int rows_p, int cols_p, int gated_I,
                                   uint8_t* q, uint8_t* s, cudaStream_t st);
+cudaError_t launch_pack_blocks_mx4(const float* src, int E, int rows_src, int cols, int rows_p, int cols_p,
+                                   int gated_I, uint8_t* q, uint8_t* s, cudaStream_t st);
 cudaError_t launch_quantize_rows_mx(const float* in, int rows, int cols, int ld_in, uint8_t* q, uint8_t* s,
                                     cudaStream_t st);
 cudaError_t launch_bounded_wait_test(uint64_t timeout_ns, int arrivals, uint32_t* result, cudaStream_t st);
@@ -155,7 +157,8 @@ cudaError_t launch_gemm_down_decode(const CUtensorMap& tmW, const CUtensorMap& t
                                     cudaStream_t st);
 
 // tmX: activation rows (prefill: 128-row boxes, decode: kDecXBoxRows-row boxes); tmW: blocked weights
-cudaError_t launch_gemm_mx(bool gated, bool decode, const CUtensorMap& tmX, const CUtensorMap& tmW,
+// fp4w: the weight codes are E2M1 (MXFP4), loaded through a 16U4_ALIGN16B tensor map.
+cudaError_t launch_gemm_mx(bool gated, bool decode, bool fp4w, const CUtensorMap& tmX, const CUtensorMap& tmW,
                            const MxGemmParams& p, int grid, cudaStream_t st);
 
 }  // namespace moe

@@ -715,6 +715,86 @@ cudaError_t launch_pack_blocks_mx(const float* src, int E, int rows_src, int col
     return cudaGetLastError();
 }
 
+// ============================================== MXFP4 weight packer
+// OCP MX v1.0 with FP4 E2M1 elements (section 5.3.3): magnitudes 0, 0.5, 1,
+// 1.5, 2, 3, 4, 6 (codes 0-7), the sign in bit 3, no infinities or NaN.
+// Nearest value, ties to the even code (the midpoints 0.25, 1.25, 2.5 and 5
+// round down, 0.75, 1.75 and 3.5 up), magnitudes above 6 saturate to 6; the
+// sign of v is kept where it rounds to 0.
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+    const float a = fabsf(v);
+    const uint32_t c = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+                       (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
+    return c | ((__float_as_uint(v) >> 28) & 8u);
+}
+
+// Shared exponent of a 32-group (section 6.3): X = floor(log2(amax)) - 2 (2 =
+// the exponent of E2M1's largest normal, 6 = 1.5 * 2^2), clamped to [-127,
+// 127], stored as X + 127; for a normal amax with biased fp32 exponent b that
+// is b - 2, every amax below 2^-125 lands on the clamp (byte 0), and an
+// all-zero group gets byte 0 with +0 codes.
+__device__ __forceinline__ uint32_t mx4_scale_byte(float amax) {
+    const int b = (int)((__float_as_uint(amax) >> 23) & 0xffu);
+    return amax == 0.0f ? 0u : (uint32_t)max(b - 2, 0);
+}
+
+// fp32 masters -> blocked E2M1 codes, two per byte (value 2j in the low
+// nibble of byte j), one 128 x 64-byte block per (row block, K block), and the
+// same 512-byte scale atoms as the MXFP8 packer.  Thread layout as
+// pack_blocks_mx_kernel: two threads per row, 64 columns (two groups) each.
+__global__ void __launch_bounds__(256) pack_blocks_mx4_kernel(const float* __restrict__ src, int rows_src, int cols,
+                                                              int rows_p, int cols_p, int gated_I,
+                                                              uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+    const int bj = blockIdx.x, bi = blockIdx.y, e = blockIdx.z;
+    const int r_local = threadIdx.x >> 1, half = threadIdx.x & 1;
+    const int dr = bi * 128 + r_local;
+    const int c0 = bj * 128 + half * 64;
+    int sr;
+    if (gated_I > 0) {
+        const int Ip = rows_p / 2;
+        sr = dr < Ip ? (dr < gated_I ? dr : -1) : (dr - Ip < gated_I ? gated_I + dr - Ip : -1);
+    } else {
+        sr = dr < rows_src ? dr : -1;
+    }
+    const float* row = sr >= 0 ? src + ((size_t)e * rows_src + sr) * cols : nullptr;
+    const size_t blk = ((size_t)e * (rows_p / 128) + bi) * (cols_p / 128) + bj;
+    uint32_t packed[8];
+    uint32_t bytes = 0;
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        float v[32];
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int c = c0 + 32 * g + i;
+            v[i] = (row && c < cols) ? __ldg(row + c) : 0.f;
+            amax = fmaxf(amax, fabsf(v[i]));
+        }
+        const uint32_t sb = mx4_scale_byte(amax);
+        const float inv = mx_inv_scale(sb);
+        const uint32_t keep = mx_keep(amax);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) word |= e2m1_code(mx_scaled(v[8 * w + i], inv, keep)) << (4 * i);
+            packed[4 * g + w] = word;
+        }
+        bytes |= sb << (8 * g);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(q + blk * 8192 + (size_t)r_local * 64 + half * 32);
+    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    *reinterpret_cast<uint16_t*>(s + blk * kMxAtomBytes + mx_atom_byte(r_local, 2 * half)) = (uint16_t)bytes;
+}
+
+cudaError_t launch_pack_blocks_mx4(const float* src, int E, int rows_src, int cols, int rows_p, int cols_p,
+                                   int gated_I, uint8_t* q, uint8_t* s, cudaStream_t st) {
+    dim3 grid(cols_p / 128, rows_p / 128, E);
+    pack_blocks_mx4_kernel<<<grid, 256, 0, st>>>(src, rows_src, cols, rows_p, cols_p, gated_I, q, s);
+    return cudaGetLastError();
+}
+
 // ============================================== stand-alone 1x32 quantiser
 // fp32 [rows, cols] -> codes [rows, cp], scale bytes [rows, cp/32] (row-major,
 // cp = cols padded to 128); one warp per 128-wide block, 8 lanes per group.

@@ -38,9 +38,10 @@ class Layer:
     """Inputs of one layer shape: host arrays (bf16 as uint16 bits) plus device tensors."""
 
     def __init__(self, cfg: synth.LayerConfig, x: np.ndarray | None = None, rw=None, rb=None, b13=None, b2=None,
-                 w13_master=None, w2_master=None, mx: bool = False):
+                 w13_master=None, w2_master=None, mx: bool = False, fp4: bool = False):
         self.cfg = cfg
-        self.mx = mx  # MXFP8 variant (1x32 UE8M0 scales) instead of 128x128 / 1x128 fp32 scales
+        self.mx = mx or fp4  # MX variant (1x32 UE8M0 scales) instead of 128x128 / 1x128 fp32 scales
+        self.fp4 = fp4  # MXFP4 weights (E2M1 codes), MXFP8 activations
         self.T, self.H, self.I, self.E, self.k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k
         self.Hp, self.Ip = cfg.Hp, cfg.Ip
         self.x = synth.layer_x(cfg) if x is None else x
@@ -74,15 +75,17 @@ class Layer:
         self.d_rb = bf16_np_to_torch(self.rb)
         self.d_b13 = bf16_np_to_torch(self.b13)
         self.d_b2 = bf16_np_to_torch(self.b2)
-        self.d_w13 = torch.empty(moe.w13_shape(E, H, I), dtype=torch.uint8, device=dev)
-        self.d_w2 = torch.empty(moe.w2_shape(E, H, I), dtype=torch.uint8, device=dev)
+        q13_shape, q2_shape = ((moe.w13_shape_fp4, moe.w2_shape_fp4) if self.fp4 else (moe.w13_shape, moe.w2_shape))
+        self.d_w13 = torch.empty(q13_shape(E, H, I), dtype=torch.uint8, device=dev)
+        self.d_w2 = torch.empty(q2_shape(E, H, I), dtype=torch.uint8, device=dev)
         if self.mx:
             self.d_s13 = torch.empty(moe.s13_mx_shape(E, H, I), dtype=torch.uint8, device=dev)
             self.d_s2 = torch.empty(moe.s2_mx_shape(E, H, I), dtype=torch.uint8, device=dev)
         else:
             self.d_s13 = torch.empty((E, 2 * Ip // 128, Hp // 128), dtype=torch.float32, device=dev)
             self.d_s2 = torch.empty((E, Hp // 128, Ip // 128), dtype=torch.float32, device=dev)
-        pack = moe.pack_weights_into_mx if self.mx else moe.pack_weights_into
+        pack = (moe.pack_weights_into_mxfp4 if self.fp4 else
+                moe.pack_weights_into_mx if self.mx else moe.pack_weights_into)
         for e0 in range(0, E, chunk_experts):
             n = min(chunk_experts, E - e0)
             m13 = torch.from_numpy(self.w13_master(e0, n)).to(dev)
@@ -116,7 +119,8 @@ class Layer:
                             np.zeros((E, Hp, Ip), np.uint8), np.ones((E, Hp // 128, Ip // 128), np.float32), set())
         q13, s13, q2, s2, done = self._oq
         todo = sorted(set(int(e) for e in experts) - done)
-        p13, p2 = (oracle.mx_pack_w13, oracle.mx_pack_w2) if self.mx else (oracle.pack_w13, oracle.pack_w2)
+        p13, p2 = ((oracle.mx4_pack_w13, oracle.mx4_pack_w2) if self.fp4 else
+                   (oracle.mx_pack_w13, oracle.mx_pack_w2) if self.mx else (oracle.pack_w13, oracle.pack_w2))
 
         def one(e):
             p13(self.w13_master(e, 1), q13[e:e + 1], s13[e:e + 1])
@@ -145,7 +149,7 @@ class Layer:
         q13, s13, q2, s2 = self.oracle_weights(np.unique(idx_all[tokens]))
         chunks = [c for c in np.array_split(tokens, max(1, min(len(tokens), threads()))) if len(c)]
 
-        fwd = oracle.mx_forward if self.mx else oracle.forward
+        fwd = oracle.mx4_forward if self.fp4 else oracle.mx_forward if self.mx else oracle.forward
 
         def one(c):
             return fwd(self.x, self.rw, self.rb, q13, s13, self.b13, q2, s2, self.b2, self.k, tokens=c,
