@@ -17,7 +17,11 @@
 //   warp 0      TMA producer: A (activation rows of one expert) and B (the
 //               expert's weight rows) per K block into a STAGES-deep ring.
 //   warp 1      TMEM allocator and MMA issuer (one thread): 4 MMAs of K=32
-//               per K block into TMEM buffer kb % NBUF, then commits.
+//               per K block into TMEM buffer kb % NBUF, then one commit to
+//               the buffer's full barrier.  That commit also frees the K
+//               block's smem stage: the first promotion warp releases the
+//               stage when it sees the buffer full (one commit per K block
+//               instead of two keeps the issuing thread on the MMAs).
 //   warp 2      metadata: stages each tile's bias in shared memory one tile ahead
 //   warp 3      idle (warpgroup 0 gives registers to the promotion warpgroups)
 //   warps 4-11  promotion + epilogue: tcgen05.ld the partial, FMA with the
@@ -214,8 +218,8 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 uint32_t ph = (s < stage) ? phase : phase ^ 1u;  // parity of that stage's last fill
                 if (filled & (1u << s)) mbar_wait(smem_u32(&full_bar[s]), ph, &dummy, err, kErrTimeoutProducer);
             }
-            // ... and, on the normal path, every stage was released by the MMA
-            // commit, so no asynchronous arrive can land after this CTA exits.
+            // ... and, on the normal path, every stage was released by the
+            // promotion warp, so no arrive can land after this CTA exits.
             if (ok) {
                 for (int i = 0; i < C::STAGES; ++i) {
                     if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) break;
@@ -254,7 +258,6 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                                  k4 > 0 ? 1u : 0u);
                     mma_commit(smem_u32(&tfull_bar[buf]));
                     if (!ok) break;
-                    mma_commit(smem_u32(&empty_bar[stage]));
                     if (++stage == C::STAGES) {
                         stage = 0;
                         sphase ^= 1u;
@@ -316,6 +319,7 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
         const int row = quarter * 32 + lane;
         const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
         int buf = 0;
+        int e_stage = 0;
         uint32_t tphase = 0;
         uint32_t tpar = 0;  // parity of the tiles this CTA has finished
         bool ok = true;
@@ -363,6 +367,9 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                     break;
                 }
                 tc_fence_after();
+                // the MMAs of this K block have completed, so its smem stage is free
+                if (warp == 4 && lane == 0) mbar_arrive(smem_u32(&empty_bar[e_stage]));
+                if (++e_stage == C::STAGES) e_stage = 0;
                 if (active) {
 #pragma unroll
                     for (int c = 0; c < 2 * C::HALVES; ++c) {  // 32-column pieces of each 128-column block
