@@ -113,6 +113,22 @@ bool make_map_fp4(CUtensorMap* m, const void* base, uint64_t rows) {
     return r == CUDA_SUCCESS;
 }
 
+// 2D bf16 tensor [rows, cols] (row stride cols * 2 bytes, a multiple of 16),
+// box 64 values (128 bytes) x box_rows, 128-byte swizzle; rows of the box past
+// the tensor read as zeros.
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int num_sms() {
     int dev = 0, n = 0;
     cudaGetDevice(&dev);
@@ -283,7 +299,15 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     rp.tiles1 = reinterpret_cast<int32_t*>(ws + L.tiles1);
     rp.tiles2 = reinterpret_cast<int32_t*>(ws + L.tiles2);
     rp.status = reinterpret_cast<uint32_t*>(ws + L.status);
-    if (launch_router(rp, st) != cudaSuccess) return MOE_ERR_CUDA;
+    // large batches with 16-byte aligned rows: the tensor-core router
+    if (const int np = router_tc_experts(T, H, E)) {
+        CUtensorMap tmX, tmW;
+        if (!make_map_bf16(&tmX, x, T, H, 128) || !make_map_bf16(&tmW, router_w, E, H, (uint32_t)np))
+            return MOE_ERR_CUDA;
+        if (launch_router_tc(rp, tmX, tmW, st) != cudaSuccess) return MOE_ERR_CUDA;
+    } else if (launch_router(rp, st) != cudaSuccess) {
+        return MOE_ERR_CUDA;
+    }
     mark(1);
 
     PermuteParams pp;

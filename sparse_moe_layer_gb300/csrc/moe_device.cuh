@@ -323,6 +323,25 @@ __device__ __forceinline__ void mma_e4m3(uint32_t tmem_d, uint64_t adesc, uint64
         : "memory");
 }
 
+// Instruction descriptor: kind::f16, A = B = bf16, D = fp32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4)                       // D format fp32
+           | (1u << 7) | (1u << 10)        // A, B format bf16
+           | ((uint32_t)(N >> 3) << 17)    // N / 8
+           | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// D (+)= A * B^T with 16-bit operands (K = 16 per instruction).
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Block-scaled MMA (kind::mxf8f6f4, one UE8M0 scale per 32 K values of each
 // A row and each B column): instruction descriptor without the scale ids
 // (A = B = e4m3, fp32 D, both K-major, bit 23 = UE8M0 scales) ...

@@ -139,8 +139,10 @@ __device__ __forceinline__ bool last_to_arrive(int* ctr, int total) {
     return s_last != 0;
 }
 
-// ---- router: 32 tokens x all experts per cluster, K split over its CTAs ----
-// A cluster of KS CTAs owns a tile of 32 tokens; CTA r of it accumulates the
+// ---- router: a token tile x all experts per cluster, K split over its CTAs ----
+// A cluster of KS CTAs owns a tile of TOK tokens (32 for decode-sized batches,
+// 128 -- 64 beyond 128 experts -- for large ones, so that each tile reads the
+// router weights once for more tokens); CTA r of it accumulates the
 // logits of all experts over its own run of 64-wide K chunks on bf16 mma.sync
 // (fp32 accumulation), with kRtNB chunks of x and router weights in flight.
 // The KS partial tiles are then summed in rank order through distributed
@@ -148,7 +150,9 @@ __device__ __forceinline__ bool last_to_arrive(int* ctr, int total) {
 // tokens r, r + KS, ...: bias, top-k and softmax for one token per warp.  So
 // small batches spread over up to 8x more SMs than they have token tiles, and
 // no partial logit goes through global memory.
-constexpr int kRtTok = 32;  // tokens per cluster
+constexpr int kRtTok = 32;      // tokens per cluster, decode-sized batches
+constexpr int kRtTokBig = 128;  // tokens per cluster, large batches (64 beyond 128 experts)
+constexpr int kRtBigT = 2048;   // batches of at least this many tokens take the large tile
 constexpr int kRtK = 64;    // K chunk
 constexpr int kRtLd = 72;   // padded smem row (bf16 elements): conflict-free fragment loads
 constexpr int kRtNB = 4;    // chunks in flight per CTA
@@ -166,25 +170,26 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int NTW>
+template <int NTW, int TOK>
 struct RouterCfg {
     static constexpr int EP = 64 * NTW;                   // experts padded to 8 warps x NTW n8 tiles
-    static constexpr int CHUNK = (kRtTok + EP) * kRtLd;   // bf16 elements of one staged K chunk
+    static constexpr int CHUNK = (TOK + EP) * kRtLd;      // bf16 elements of one staged K chunk
     static constexpr int LDL = EP + 4;                    // fp32 row of a logit tile
     static constexpr size_t LOAD_BYTES = (size_t)kRtNB * CHUNK * 2;
-    static constexpr size_t TILE_BYTES = (size_t)2 * kRtTok * LDL * 4;  // partial + finished logits
+    static constexpr size_t TILE_BYTES = (size_t)2 * TOK * LDL * 4;  // partial + finished logits
     static constexpr size_t SMEM = LOAD_BYTES > TILE_BYTES ? LOAD_BYTES : TILE_BYTES;
 };
 
 // cpc: K chunks per CTA.  VEC: H % 8 == 0 (16-byte cp.async rows).
-template <int NTW, bool VEC>
+template <int NTW, bool VEC, int TOK>
 __global__ void __launch_bounds__(256) router_kernel(RouteParams p, int cpc) {
-    using C = RouterCfg<NTW>;
+    using C = RouterCfg<NTW, TOK>;
+    constexpr int MT = TOK / 16;  // m16 tiles of tokens (every warp covers all of them)
     constexpr int EP = C::EP, LDL = C::LDL;
     extern __shared__ __align__(16) uint8_t smem[];
     uint16_t* cbuf = reinterpret_cast<uint16_t*>(smem);  // [kRtNB][(kRtTok + EP) * kRtLd]
     const uint32_t rank = cluster_ctarank(), KS = cluster_nctarank();
-    const int t0 = (int)cluster_id_x() * kRtTok;
+    const int t0 = (int)cluster_id_x() * TOK;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, c = lane & 3;
     const int nchunk = (p.H + kRtK - 1) / kRtK;
@@ -192,31 +197,31 @@ __global__ void __launch_bounds__(256) router_kernel(RouteParams p, int cpc) {
     const int nmine = max(0, min(cpc, nchunk - c0));
 
     auto load_chunk = [&](int ch, int buf) {
-        uint16_t* xs = cbuf + buf * C::CHUNK;  // [kRtTok][kRtLd] then [EP][kRtLd]
+        uint16_t* xs = cbuf + buf * C::CHUNK;  // [TOK][kRtLd] then [EP][kRtLd]
         const int k0 = ch * kRtK;
         if (VEC) {
-            for (int i = tid; i < (kRtTok + EP) * 8; i += 256) {
+            for (int i = tid; i < (TOK + EP) * 8; i += 256) {
                 const int r = i >> 3, q = i & 7, k = k0 + q * 8;
-                const bool isx = r < kRtTok;
-                const int row = isx ? t0 + r : r - kRtTok;
+                const bool isx = r < TOK;
+                const int row = isx ? t0 + r : r - TOK;
                 const bool ok = (isx ? row < p.T : row < p.E) && k < p.H;
                 const uint16_t* src = isx ? p.x + (size_t)row * p.H + k : p.rw + (size_t)row * p.H + k;
                 cp_async16(smem_u32(xs + r * kRtLd + q * 8), ok ? src : p.x, ok);
             }
         } else {
-            for (int i = tid; i < (kRtTok + EP) * kRtK; i += 256) {
+            for (int i = tid; i < (TOK + EP) * kRtK; i += 256) {
                 const int r = i / kRtK, q = i - r * kRtK, k = k0 + q;
-                const bool isx = r < kRtTok;
-                const int row = isx ? t0 + r : r - kRtTok;
+                const bool isx = r < TOK;
+                const int row = isx ? t0 + r : r - TOK;
                 const bool ok = (isx ? row < p.T : row < p.E) && k < p.H;
                 xs[r * kRtLd + q] = ok ? (isx ? p.x[(size_t)row * p.H + k] : p.rw[(size_t)row * p.H + k]) : (uint16_t)0;
             }
         }
     };
 
-    float acc[2][NTW][4];
+    float acc[MT][NTW][4];
 #pragma unroll
-    for (int m = 0; m < 2; ++m)
+    for (int m = 0; m < MT; ++m)
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
@@ -233,13 +238,13 @@ __global__ void __launch_bounds__(256) router_kernel(RouteParams p, int cpc) {
         asm volatile("cp.async.wait_group %0;" ::"n"(kRtNB - 1) : "memory");
         __syncthreads();
         const uint16_t* xb = cbuf + buf * C::CHUNK;
-        const uint16_t* wb = xb + kRtTok * kRtLd;
+        const uint16_t* wb = xb + TOK * kRtLd;
 #pragma unroll
         for (int ks = 0; ks < kRtK / 16; ++ks) {
             const int kk = ks * 16 + 2 * c;
-            uint32_t a[2][4];
+            uint32_t a[MT][4];
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
+            for (int m = 0; m < MT; ++m) {
                 const uint16_t* r0 = xb + (m * 16 + g) * kRtLd;
                 const uint16_t* r1 = r0 + 8 * kRtLd;
                 a[m][0] = *reinterpret_cast<const uint32_t*>(r0 + kk);
@@ -253,7 +258,7 @@ __global__ void __launch_bounds__(256) router_kernel(RouteParams p, int cpc) {
                 const uint32_t b0 = *reinterpret_cast<const uint32_t*>(br + kk);
                 const uint32_t b1 = *reinterpret_cast<const uint32_t*>(br + kk + 8);
 #pragma unroll
-                for (int m = 0; m < 2; ++m) mma_bf16_16816(acc[m][j], a[m], b0, b1);
+                for (int m = 0; m < MT; ++m) mma_bf16_16816(acc[m][j], a[m], b0, b1);
             }
         }
         __syncthreads();
@@ -264,10 +269,10 @@ __global__ void __launch_bounds__(256) router_kernel(RouteParams p, int cpc) {
     __syncthreads();
 
     // this CTA's partial logits (no bias) into shared memory, visible to the cluster
-    float* part = reinterpret_cast<float*>(smem);  // [kRtTok][LDL]
-    float* lg = part + kRtTok * LDL;                // [ceil(kRtTok / KS)][LDL]
+    float* part = reinterpret_cast<float*>(smem);  // [TOK][LDL]
+    float* lg = part + TOK * LDL;                   // [ceil(TOK / KS)][LDL]
 #pragma unroll
-    for (int m = 0; m < 2; ++m)
+    for (int m = 0; m < MT; ++m)
 #pragma unroll
         for (int j = 0; j < NTW; ++j) {
             const int col = (warp * NTW + j) * 8 + 2 * c;
@@ -279,7 +284,7 @@ __global__ void __launch_bounds__(256) router_kernel(RouteParams p, int cpc) {
         }
     cluster_sync_all();
     // tokens rank, rank + KS, ...: sum the KS partials in rank order, add the bias
-    const int nmy = (kRtTok - (int)rank + (int)KS - 1) / (int)KS;
+    const int nmy = (TOK - (int)rank + (int)KS - 1) / (int)KS;
     for (int idx = tid; idx < nmy * EP; idx += 256) {
         const int li = idx / EP, e = idx - li * EP;
         const int r = (int)rank + li * (int)KS;
@@ -301,17 +306,20 @@ __global__ void __launch_bounds__(256) router_kernel(RouteParams p, int cpc) {
     if (p.scan_in_router && last_to_arrive(p.done, gridDim.x)) finish_scan(p);
 }
 
-template <int NTW, bool VEC>
+template <int NTW, bool VEC, int TOK>
 static cudaError_t launch_router_t(const RouteParams& p, cudaStream_t st) {
-    using C = RouterCfg<NTW>;
-    const int ntiles = (p.T + kRtTok - 1) / kRtTok;
+    using C = RouterCfg<NTW, TOK>;
+    const int ntiles = (p.T + TOK - 1) / TOK;
     const int nchunk = (p.H + kRtK - 1) / kRtK;
-    int ks = ntiles >= 148 ? 1 : 296 / ntiles;  // about two CTAs per SM in all
+    // about two CTAs per SM in all with the small tile; one (shared memory)
+    // with the large one
+    const int want = TOK == kRtTok ? 296 : 152;
+    int ks = ntiles >= want / 2 ? 1 : want / ntiles;
     ks = ks < 1 ? 1 : (ks > 8 ? 8 : ks);
     if (ks > nchunk) ks = nchunk;
     const int cpc = (nchunk + ks - 1) / ks;
     ks = (nchunk + cpc - 1) / cpc;  // no CTA without a chunk
-    cudaError_t e = cudaFuncSetAttribute(router_kernel<NTW, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(router_kernel<NTW, VEC, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -326,16 +334,240 @@ static cudaError_t launch_router_t(const RouteParams& p, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, router_kernel<NTW, VEC>, p, cpc);
+    return cudaLaunchKernelEx(&cfg, router_kernel<NTW, VEC, TOK>, p, cpc);
 }
 
 bool router_scans(int T) { return T >= 512; }
 
+template <int NTW, int TOK>
+static cudaError_t launch_router_v(const RouteParams& p, cudaStream_t st) {
+    return (p.H % 8) == 0 ? launch_router_t<NTW, true, TOK>(p, st) : launch_router_t<NTW, false, TOK>(p, st);
+}
+
 cudaError_t launch_router(const RouteParams& p, cudaStream_t st) {
-    const bool vec = (p.H % 8) == 0;
-    if (p.E <= 64) return vec ? launch_router_t<1, true>(p, st) : launch_router_t<1, false>(p, st);
-    if (p.E <= 128) return vec ? launch_router_t<2, true>(p, st) : launch_router_t<2, false>(p, st);
-    return vec ? launch_router_t<4, true>(p, st) : launch_router_t<4, false>(p, st);
+    const bool big = p.T >= kRtBigT;
+    if (p.E <= 64) return big ? launch_router_v<1, kRtTokBig>(p, st) : launch_router_v<1, kRtTok>(p, st);
+    if (p.E <= 128) return big ? launch_router_v<2, kRtTokBig>(p, st) : launch_router_v<2, kRtTok>(p, st);
+    return big ? launch_router_v<4, kRtTokBig / 2>(p, st) : launch_router_v<4, kRtTok>(p, st);
+}
+
+// ---- router on the tensor cores: large batches with 16-byte aligned rows ----
+// One CTA per 128-token tile.  TMA brings 64-wide K chunks of the tile's x
+// rows and of every router weight row (experts padded to NP, the padding
+// zero-filled) into a ring; one thread issues tcgen05.mma kind::f16 (bf16 x
+// bf16, fp32 accumulator in TMEM; M = 128 tokens, N = NP experts, K = 16 per
+// instruction).  After the last chunk four warps each read the logits of 32
+// tokens (TMEM lane = token), add the bias, keep the 8 largest in registers
+// (ties -> lower expert index: experts are visited in ascending order and only
+// a strictly larger logit moves ahead), and write the softmax over the first k
+// of them in ascending expert order -- the same selection and arithmetic as
+// the cluster kernel above, whose mma.sync path runs far below the tensor
+// cores' rate on this part.
+template <int NP>
+struct RouterTcCfg {
+    static constexpr int A_BYTES = 128 * 128;  // 128 tokens x 64 bf16
+    static constexpr int B_BYTES = NP * 128;   // NP experts x 64 bf16
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = NP > 128 ? 4 : 6;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+    static constexpr int TMEM_COLS = NP < 32 ? 32 : NP;  // a power of two >= 32
+    static constexpr uint32_t IDESC = idesc_bf16_f32(128, NP);
+    static_assert(NP % 32 == 0 && NP <= 256, "expert padding");
+};
+
+template <int NP>
+__global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                           const __grid_constant__ CUtensorMap tmW, RouteParams p) {
+    using C = RouterTcCfg<NP>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    __shared__ __align__(8) uint64_t full_bar[C::STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
+    __shared__ __align__(8) uint64_t dfull_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    __shared__ float s_bias[NP];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = blockIdx.x * 128;
+    const int nchunk = (p.H + 63) / 64;
+    if (tid == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        mbar_init(smem_u32(&dfull_bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), C::TMEM_COLS);
+    for (int e = tid; e < NP; e += blockDim.x) s_bias[e] = e < p.E ? bf16_bits_to_f32(p.rb[e]) : 0.f;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    volatile int* abort_p = &abort_flag;
+    uint32_t* err = p.status + kStatusError;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int c = 0;
+            for (; c < nchunk; ++c) {
+                const int stage = c % C::STAGES;
+                const uint32_t phase = (uint32_t)(c / C::STAGES) & 1u;
+                if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) break;
+                const uint32_t fb = smem_u32(&full_bar[stage]);
+                mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                const uint32_t a_dst = smem_u32(smem + stage * C::STAGE_BYTES);
+                tma_load_2d(a_dst, &tmX, c * 64, t0, fb);
+                tma_load_2d(a_dst + C::A_BYTES, &tmW, c * 64, 0, fb);
+            }
+            // the last fill of every stage has landed before the CTA may exit
+            int dummy = 0;
+            for (int q = max(0, c - C::STAGES); q < c; ++q)
+                mbar_wait(smem_u32(&full_bar[q % C::STAGES]), (uint32_t)(q / C::STAGES) & 1u, &dummy, err,
+                          kErrTimeoutProducer);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------- MMA issuer
+            for (int c = 0; c < nchunk; ++c) {
+                const int stage = c % C::STAGES;
+                if (!mbar_wait(smem_u32(&full_bar[stage]), (uint32_t)(c / C::STAGES) & 1u, abort_p, err,
+                               kErrTimeoutMma))
+                    break;
+                tc_fence_after();
+                const uint32_t a_base = smem_u32(smem + stage * C::STAGE_BYTES);
+                const uint32_t b_base = a_base + C::A_BYTES;
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4)
+                    mma_bf16(tmem, smem_desc_sw128(a_base + 32 * k4), smem_desc_sw128(b_base + 32 * k4), C::IDESC,
+                             (c | k4) != 0 ? 1u : 0u);
+                mma_commit(smem_u32(&empty_bar[stage]));
+            }
+            // the accumulator is complete (or, after an abort, every issued MMA has
+            // finished) once this commit lands
+            mma_commit(smem_u32(&dfull_bar));
+            int dummy = 0;
+            mbar_wait(smem_u32(&dfull_bar), 0, &dummy, err, kErrTimeoutMma);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------ selection + softmax
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int row = quarter * 32 + lane;
+        const int t = t0 + row;
+        const bool ok = mbar_wait(smem_u32(&dfull_bar), 0, abort_p, err, kErrTimeoutEpilogue);
+        tc_fence_after();
+        if (ok) {
+            float v[kMaxTopK];
+            int id[kMaxTopK];
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j) {
+                v[j] = -INFINITY;
+                id[j] = 0x7fffffff;
+            }
+            const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll 1
+            for (int c0 = 0; c0 < NP; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(t_lane + (uint32_t)c0, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int e = c0 + i;
+                    const float l = __uint_as_float(r[i]) + s_bias[e];
+                    if (e < p.E && l > v[kMaxTopK - 1]) {
+                        // insert, keeping v descending; an equal value stays behind
+                        float cv = l;
+                        int ci = e;
+#pragma unroll
+                        for (int j = 0; j < kMaxTopK; ++j) {
+                            const bool gt = cv > v[j];
+                            const float tv = v[j];
+                            const int ti = id[j];
+                            v[j] = gt ? cv : tv;
+                            id[j] = gt ? ci : ti;
+                            cv = gt ? tv : cv;
+                            ci = gt ? ti : ci;
+                        }
+                    }
+                }
+            }
+            if (t < p.T) {
+                const int k = p.k;
+                // the first k in ascending expert order (the rest sort behind them)
+#pragma unroll
+                for (int j = 0; j < kMaxTopK; ++j)
+                    if (j >= k) id[j] = 0x7fffffff;
+#pragma unroll
+                for (int a = 0; a < kMaxTopK; ++a)
+#pragma unroll
+                    for (int b = 0; b + 1 < kMaxTopK - a; ++b) {
+                        const bool sw = id[b] > id[b + 1];
+                        const int ib = id[b], ib1 = id[b + 1];
+                        const float vb = v[b], vb1 = v[b + 1];
+                        id[b] = sw ? ib1 : ib;
+                        id[b + 1] = sw ? ib : ib1;
+                        v[b] = sw ? vb1 : vb;
+                        v[b + 1] = sw ? vb : vb1;
+                    }
+                float m = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < kMaxTopK; ++j)
+                    if (j < k) m = fmaxf(m, v[j]);
+                float z = 0.f;
+#pragma unroll
+                for (int j = 0; j < kMaxTopK; ++j)
+                    if (j < k) z += expf(v[j] - m);
+#pragma unroll
+                for (int j = 0; j < kMaxTopK; ++j) {
+                    if (j < k) {
+                        const float w = expf(v[j] - m) / z;
+                        p.topk_idx[(size_t)t * k + j] = id[j];
+                        p.topk_w[(size_t)t * k + j] = w;
+                        __nv_bfloat16 wb = __float2bfloat16_rn(w);
+                        p.topk_wb[(size_t)t * k + j] = *reinterpret_cast<uint16_t*>(&wb);
+                        atomicAdd(&p.hist[(size_t)(t / kChunkTokens) * p.E + id[j]], 1);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+    if (p.scan_in_router && last_to_arrive(p.done, gridDim.x)) finish_scan(p);
+}
+
+template <int NP>
+static cudaError_t launch_router_tc_t(const RouteParams& p, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                                      cudaStream_t st) {
+    using C = RouterTcCfg<NP>;
+    cudaError_t e = cudaFuncSetAttribute(router_tc_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    router_tc_kernel<NP><<<(p.T + 127) / 128, 256, C::SMEM, st>>>(tmX, tmW, p);
+    return cudaGetLastError();
+}
+
+int router_tc_experts(int T, int H, int E) {
+    if (T < kRtBigT || (H % 8) != 0 || E > 256) return 0;
+    return E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256;
+}
+
+cudaError_t launch_router_tc(const RouteParams& p, const CUtensorMap& tmX, const CUtensorMap& tmW, cudaStream_t st) {
+    switch (router_tc_experts(p.T, p.H, p.E)) {
+        case 32: return launch_router_tc_t<32>(p, tmX, tmW, st);
+        case 64: return launch_router_tc_t<64>(p, tmX, tmW, st);
+        case 128: return launch_router_tc_t<128>(p, tmX, tmW, st);
+        case 256: return launch_router_tc_t<256>(p, tmX, tmW, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 // ======================================================= permute + x quant

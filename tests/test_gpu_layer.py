@@ -173,8 +173,19 @@ def test_equal_logits_pick_lowest_experts(moe):
 
 def test_many_tokens_router_scan_and_blocked_permute(moe):
     # T >= 512: the router's last CTA scans the histogram; T > 2048: 8 tokens per permutation CTA;
-    # 79 token tiles: router clusters of 2 CTAs, 2 of the 4 K chunks each
+    # T >= 2048: 128-token router tiles, 20 of them (the last holds 68 tokens), clusters of 4 CTAs
+    # with one K chunk each
     full_check(moe, _adhoc("many_tokens", 2500, 256, 256, 8, 2), n_sample=48)
+
+
+def test_router_scan_with_small_token_tiles(moe):
+    # 512 <= T < 2048: the router's last CTA scans, 32-token tiles (32 of them, the last holds 8)
+    full_check(moe, _adhoc("mid_tokens", 1000, 256, 256, 8, 2), n_sample=32)
+
+
+def test_large_router_tile_with_unaligned_rows(moe):
+    # 128-token router tiles fed by element-wise loads (H not a multiple of 8), a ragged last tile
+    full_check(moe, _adhoc("many_odd", 2100, 196, 136, 6, 2), n_sample=32)
 
 
 def test_hidden_size_not_multiple_of_8(moe):
