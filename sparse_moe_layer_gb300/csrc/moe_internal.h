@@ -133,9 +133,9 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 bool router_scans(int T);  // large batches: the router scans, small ones: the permutation kernel
 cudaError_t launch_router(const RouteParams& p, cudaStream_t st);
-// Tensor-core router for large batches: the padded expert count NP it would use
-// (32, 64, 128 or 256), or 0 when the batch takes the cluster kernel above
-// (small T, rows not 16-byte aligned, more than 256 experts).  tmX / tmW are
+// Tensor-core router: the padded expert count NP it would use (32, 64, 128 or
+// 256), or 0 when the layer takes the cluster kernel above (fewer than 2048
+// tokens, rows not 16-byte aligned, more than 256 experts).  tmX / tmW are
 // bf16 tensor maps of x [T, H] and the router weights [E, H] with 64 x 128 and
 // 64 x NP boxes (128-byte swizzle).
 int router_tc_experts(int T, int H, int E);

@@ -188,6 +188,20 @@ def test_large_router_tile_with_unaligned_rows(moe):
     full_check(moe, _adhoc("many_odd", 2100, 196, 136, 6, 2), n_sample=32)
 
 
+@pytest.mark.parametrize("E,k", [(64, 8), (200, 8)])
+def test_router_expert_paddings(moe, E, k):
+    # the tensor-core router pads the experts to 64 and 256 columns (zero-filled weight rows)
+    full_check(moe, _adhoc(f"experts_{E}", 2100, 256, 128, E, k), n_sample=16)
+
+
+def test_equal_logits_pick_lowest_experts_large_batch(moe):
+    layer = _adhoc("ties_large", 2048, 256, 128, 16, 4, rb=np.zeros(16, np.float32), rw_zero=True)
+    layer.to_device()
+    _, v, _ = layer.run_gpu()
+    assert np.all(v["topk_idx"].cpu().numpy() == [0, 1, 2, 3])
+    assert np.allclose(v["topk_w"].cpu().numpy(), 0.25, rtol=1e-6)
+
+
 def test_hidden_size_not_multiple_of_8(moe):
     # rows of x and of the router weights are not 16-byte aligned: element-wise router loads
     full_check(moe, _adhoc("odd_hidden", 19, 196, 136, 6, 2))
