@@ -89,11 +89,21 @@ __device__ __forceinline__ void write_route(const RouteParams& p, int t, const f
 }
 
 // Run by the last CTA (blockDim 256): counts, offsets, chunk bases, tile lists.
-__device__ void finish_scan(const RouteParams& p) {
+// The (chunk, expert) histogram is first copied into `buf` (the CTA's shared
+// memory, free by then) with coalesced loads when it fits in `cap` ints, so
+// the per-expert sums over the chunks run from shared memory instead of one
+// dependent L2 round trip per chunk.
+__device__ void finish_scan(const RouteParams& p, int* buf, int cap) {
     __shared__ int s_count[kMaxExperts], s_off[kMaxExperts];
+    const int n = p.nchunks * p.E;
+    const bool staged = n <= cap;
+    if (staged)
+        for (int i = threadIdx.x; i < n; i += blockDim.x) buf[i] = __ldcg(&p.hist[i]);
+    __syncthreads();
+    auto h = [&](int c, int e) { return staged ? buf[(size_t)c * p.E + e] : __ldcg(&p.hist[(size_t)c * p.E + e]); };
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
         int run = 0;
-        for (int c = 0; c < p.nchunks; ++c) run += __ldcg(&p.hist[(size_t)c * p.E + e]);
+        for (int c = 0; c < p.nchunks; ++c) run += h(c, e);
         s_count[e] = run;
     }
     __syncthreads();
@@ -123,7 +133,7 @@ __device__ void finish_scan(const RouteParams& p) {
         int run = s_off[e];
         for (int c = 0; c < p.nchunks; ++c) {
             p.chunk_base[(size_t)c * p.E + e] = run;
-            run += __ldcg(&p.hist[(size_t)c * p.E + e]);
+            run += h(c, e);
         }
     }
 }
@@ -303,7 +313,8 @@ __global__ void __launch_bounds__(256) router_kernel(RouteParams p, int cpc) {
     }
     // no CTA leaves while another may still read its partial tile
     cluster_sync_all();
-    if (p.scan_in_router && last_to_arrive(p.done, gridDim.x)) finish_scan(p);
+    if (p.scan_in_router && last_to_arrive(p.done, gridDim.x))
+        finish_scan(p, reinterpret_cast<int*>(smem), (int)(C::SMEM / 4));
 }
 
 template <int NTW, bool VEC, int TOK>
@@ -542,7 +553,8 @@ __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    if (p.scan_in_router && last_to_arrive(p.done, gridDim.x)) finish_scan(p);
+    if (p.scan_in_router && last_to_arrive(p.done, gridDim.x))
+        finish_scan(p, reinterpret_cast<int*>(smem), C::STAGES * C::STAGE_BYTES / 4);
 }
 
 template <int NP>
@@ -576,9 +588,9 @@ cudaError_t launch_router_tc(const RouteParams& p, const CUtensorMap& tmX, const
 // ======================================================= permute + x quant
 // CTA = 8 warps over `tokens_per_cta` consecutive tokens (all in one 256-token
 // chunk).  Row of (t, j) = chunk_base[chunk, e] + number of earlier tokens of
-// the chunk routed to e, so rows are sorted by (expert, token).  Then each
-// (token, 128-group) item is quantised by one warp: amax, s = amax/448,
-// code = e4m3(x/s), written to each of the token's k rows.
+// the chunk routed to e, so rows are sorted by (expert, token).  Then every
+// 128-group of the token is quantised (amax, s = amax/448, code = e4m3(x/s);
+// one warp covers four groups) and written to each of the token's k rows.
 __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
     extern __shared__ __align__(16) uint8_t psm[];
     uint16_t* xs = reinterpret_cast<uint16_t*>(psm);  // this CTA's x rows, [tokens_per_cta][Hx]
@@ -704,48 +716,72 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
     }
     __syncthreads();
 
+    // One warp item = one token x 512 columns (four 128-groups): lane l holds
+    // the 16 columns [16l, 16l+16) of the item, so lanes 8q..8q+7 hold group q
+    // (MXFP8: lane pairs hold its four 1x32 groups), and writes them to each of
+    // the token's k rows with one 16-byte store.
     const int G = p.Hp / 128;
+    const int SG = (G + 3) / 4;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int item = warp; item < nt * G; item += 8) {
-        const int tt = item / G, g = item - tt * G;
-        const int c = g * 128 + lane * 4;
-        float a[4];
-        if (c + 4 <= Hx) {
-            const uint2 v = *reinterpret_cast<const uint2*>(xs + tt * Hx + c);
-            a[0] = __uint_as_float(v.x << 16);
-            a[1] = __uint_as_float(v.x & 0xffff0000u);
-            a[2] = __uint_as_float(v.y << 16);
-            a[3] = __uint_as_float(v.y & 0xffff0000u);
+    for (int item = warp; item < nt * SG; item += 8) {
+        const int tt = item / SG, sg = item - tt * SG;
+        const int g = sg * 4 + (lane >> 3);  // this lane's 128-group
+        const int c = sg * 512 + lane * 16;  // its first column
+        const bool act = g < G;              // lanes past the row's last group only join the shuffles
+        float a[16];
+        if (c + 16 <= Hx) {
+            const uint4 v0 = *reinterpret_cast<const uint4*>(xs + tt * Hx + c);
+            const uint4 v1 = *reinterpret_cast<const uint4*>(xs + tt * Hx + c + 8);
+            const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                a[2 * i] = __uint_as_float(w[i] << 16);
+                a[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+            }
         } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = (c + i < Hx) ? bf16_bits_to_f32(xs[tt * Hx + c + i]) : 0.f;
+            for (int i = 0; i < 16; ++i) a[i] = (c + i < Hx) ? bf16_bits_to_f32(xs[tt * Hx + c + i]) : 0.f;
         }
-        float amax = fmaxf(fmaxf(fabsf(a[0]), fabsf(a[1])), fmaxf(fabsf(a[2]), fabsf(a[3])));
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(a[i]));
+        uint4 q;
+        uint32_t meta;  // MXFP8: the group's atom cell (four scale bytes); else the fp32 scale
         if (p.mx) {
-            // 1x32 groups: lanes 8q..8q+7 hold group q of this 128-wide K block
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // the lane pair's 32 values
+            const uint32_t sb = mx_scale_byte(amax);
+            const float inv = mx_inv_scale(sb);
+            const uint32_t keep = mx_keep(amax);
+            q.x = mx_quant4(a[0], a[1], a[2], a[3], inv, keep);
+            q.y = mx_quant4(a[4], a[5], a[6], a[7], inv, keep);
+            q.z = mx_quant4(a[8], a[9], a[10], a[11], inv, keep);
+            q.w = mx_quant4(a[12], a[13], a[14], a[15], inv, keep);
+            const int b = lane & ~7;
+            meta = __shfl_sync(0xffffffffu, sb, b) | (__shfl_sync(0xffffffffu, sb, b + 2) << 8) |
+                   (__shfl_sync(0xffffffffu, sb, b + 4) << 16) | (__shfl_sync(0xffffffffu, sb, b + 6) << 24);
+        } else {
 #pragma unroll
             for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const uint32_t sb = mx_scale_byte(amax);
-            const uint32_t q = mx_quant4(a[0], a[1], a[2], a[3], mx_inv_scale(sb), mx_keep(amax));
-            // the block's four scale bytes, one 32-bit cell of the row's atom
-            const uint32_t cell = __shfl_sync(0xffffffffu, sb, 0) | (__shfl_sync(0xffffffffu, sb, 8) << 8) |
-                                  (__shfl_sync(0xffffffffu, sb, 16) << 16) | (__shfl_sync(0xffffffffu, sb, 24) << 24);
+            const float sc = group_scale(amax);
+            const float rs = recip_rn(sc);
+            q.x = quant4(a[0], a[1], a[2], a[3], amax, sc, rs);
+            q.y = quant4(a[4], a[5], a[6], a[7], amax, sc, rs);
+            q.z = quant4(a[8], a[9], a[10], a[11], amax, sc, rs);
+            q.w = quant4(a[12], a[13], a[14], a[15], amax, sc, rs);
+            meta = __float_as_uint(sc);
+        }
+        if (act) {
+            const bool lead = (lane & 7) == 0;
             for (int j = 0; j < p.k; ++j) {
                 const int r = s_row[tt * p.k + j];
-                *reinterpret_cast<uint32_t*>(p.xq + (size_t)r * p.Hp + c) = q;
-                if (lane == 0)
-                    *reinterpret_cast<uint32_t*>(p.sxa + s_aoff[tt * p.k + j] + (size_t)g * kMxAtomBytes) = cell;
+                *reinterpret_cast<uint4*>(p.xq + (size_t)r * p.Hp + c) = q;
+                if (lead) {
+                    if (p.mx)
+                        *reinterpret_cast<uint32_t*>(p.sxa + s_aoff[tt * p.k + j] + (size_t)g * kMxAtomBytes) = meta;
+                    else
+                        p.sx[(size_t)g * p.R + r] = __uint_as_float(meta);  // K-block-major [Hp/128, R]
+                }
             }
-            continue;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float s = group_scale(amax);
-        const uint32_t q = quant4(a[0], a[1], a[2], a[3], amax, s, recip_rn(s));
-        for (int j = 0; j < p.k; ++j) {
-            const int r = s_row[tt * p.k + j];
-            *reinterpret_cast<uint32_t*>(p.xq + (size_t)r * p.Hp + c) = q;
-            if (lane == 0) p.sx[(size_t)g * p.R + r] = s;  // K-block-major [Hp/128, R]
         }
     }
 }
