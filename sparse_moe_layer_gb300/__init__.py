@@ -429,3 +429,34 @@ class MoeLayer:
         T = x.shape[0]
         return forward(x, self.router_w, self.router_b, self.w13, self.s13, self.b13, self.w2, self.s2, self.b2,
                        self.top_k, out=out, workspace=self.workspace(T), stream=stream)
+
+    def graphed(self, T: int) -> "GraphedMoeLayer":
+        """The layer for batches of exactly T tokens captured once as a CUDA graph
+        (see GraphedMoeLayer)."""
+        return GraphedMoeLayer(self, T)
+
+
+class GraphedMoeLayer:
+    """One batch size of a MoeLayer captured as a CUDA graph: the workspace memset
+    and the five kernels of a forward, with their programmatic dependencies.
+    `x` and `out` are the graph's static device buffers ([T, H] bf16): write the
+    batch into `x`, call, read `out`.  A call replays the graph on the current
+    stream, one launch instead of six."""
+
+    def __init__(self, layer: MoeLayer, T: int):
+        dev = layer.router_w.device
+        self.layer, self.T = layer, T
+        self.x = torch.zeros((T, layer.H), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((T, layer.H), dtype=torch.bfloat16, device=dev)
+        ws = layer.workspace(T)
+        # one eager call first: kernel attributes and tensor-map encoders are set up outside the capture
+        layer(self.x, out=self.out)
+        torch.cuda.synchronize(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            forward(self.x, layer.router_w, layer.router_b, layer.w13, layer.s13, layer.b13, layer.w2, layer.s2,
+                    layer.b2, layer.top_k, out=self.out, workspace=ws)
+
+    def __call__(self) -> torch.Tensor:
+        self.graph.replay()
+        return self.out

@@ -207,6 +207,19 @@ def test_hidden_size_not_multiple_of_8(moe):
     full_check(moe, _adhoc("odd_hidden", 19, 196, 136, 6, 2))
 
 
+def test_graphed_layer_matches_eager(moe):
+    layer = Layer(synth.config("tiny")).to_device()
+    ml = moe.MoeLayer(layer.d_rw, layer.d_rb, layer.d_w13, layer.d_s13, layer.d_b13, layer.d_w2, layer.d_s2,
+                      layer.d_b2, layer.k)
+    g = ml.graphed(layer.T)
+    for x in (layer.d_x, torch.flip(layer.d_x, dims=[0]).contiguous()):  # two batches through one graph
+        ref = ml(x)
+        g.x.copy_(x)
+        got = g()
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+
+
 def test_repeated_calls_are_bit_identical(moe):
     layer = Layer(synth.config("tiny")).to_device()
     a, _, ws = layer.run_gpu()
