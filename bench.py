@@ -278,6 +278,21 @@ def cpu_oracle_leg(cfg, seconds: float, mx: bool = False, fp4: bool = False):
     return passes * n / dt, desc, dt
 
 
+def max_over_ranks(ms: float, pg, device) -> float:
+    """The slowest rank's time (every rank receives it); the value itself on one rank."""
+    if pg is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, T: int, ms: float) -> float:
+    """Whole-job throughput: every rank's T tokens over the slowest rank's step time."""
+    return world * T / (ms * 1e-3)
+
+
 def run_reference(args, cfg, rank):
     """The oracle as the reference arm: K steps, each a bounded sample (rank 0 only)."""
     if rank != 0:
@@ -414,11 +429,7 @@ def main():
     if pg:
         pg.barrier()
     step_ms = [ev_s[i].elapsed_time(ev_e[i]) for i in range(K)]
-    ms = statistics.fmean(step_ms)
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.fmean(step_ms), pg, dev)
     # Timed region 2 (per-kernel time): the same K steps launched directly with
     # moe_forward_profiled, whose events are recorded on the launching stream
     # between the five kernels.
@@ -458,12 +469,8 @@ def main():
         out_host.copy_(glayer(), non_blocking=True)
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = statistics.fmean(a.elapsed_time(b) for a, b in e2e_ev)
+    e2e_ms = max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in e2e_ev), pg, dev)
     out = glayer.out
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
     assert torch.equal(out_host.view(torch.int16), out.cpu().view(torch.int16))
 
     pk = peaks()
@@ -495,7 +502,7 @@ def main():
     roof["peak_source"] = pk["source"] + (" (hbm_gbs)" if not prefill else " (2 x bf16_tflops_sustained)")
     roof["algorithmic_per_launch"] = alg["gemm1_bytes"] if not prefill else alg["gemm1_flops"]
 
-    value = world * T / (ms * 1e-3)
+    value = job_tokens_per_s(world, T, ms)
     line = dict(metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=K, warmup=args.warmup,
                 ms_per_step=ms, higher_is_better=True, scaling="weak", vs_baseline=None,
                 dtype="e2m1 x e4m3" if fp4 else "e4m3",
@@ -516,7 +523,7 @@ def main():
                           launch="CUDA graph replay of " + ("moe_forward_mxfp4" if fp4 else "moe_forward_mx" if mx
                                                             else "moe_forward"),
                           eager_ms_per_step=eager_ms),
-                e2e=dict(value=world * T / (e2e_ms * 1e-3), unit="tokens/s", h2d_bytes_per_step=T * H * 2,
+                e2e=dict(value=job_tokens_per_s(world, T, e2e_ms), unit="tokens/s", h2d_bytes_per_step=T * H * 2,
                          d2h_bytes_per_step=T * H * 2, ms_per_step=e2e_ms,
                          api="MoeLayer.graphed(T): x copied in from pinned host memory, one graph replay, "
                              "out copied back"),
