@@ -8,4 +8,3 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
-    config.addinivalue_line("markers", "slow: long CPU-side work (runs on the GPU box with the gpu tests)")
