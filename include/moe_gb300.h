@@ -102,8 +102,9 @@ moe_status moe_get_workspace_layout(int T, int H, int I, int E, int top_k, moe_w
  *   b2       bf16 [E, H]
  *   out      bf16 [T, H]
  *   workspace: device buffer of at least moe_workspace_size(...) bytes, 256-byte aligned.
- * All pointers are device pointers; x, router_w, w13, w2, out and the
- * workspace must be 16-byte aligned.  stream is a cudaStream_t (NULL = legacy default stream).
+ * All pointers are device pointers; x, router_w, w13, w2 and out must be 16-byte
+ * aligned, the workspace 256-byte aligned (else MOE_ERR_UNSUPPORTED).
+ * stream is a cudaStream_t (NULL = legacy default stream).
  */
 moe_status moe_forward(const void* x, const void* router_w, const void* router_b, const uint8_t* w13, const float* s13,
                        const void* b13, const uint8_t* w2, const float* s2, const void* b2, int T, int H, int I, int E,
