@@ -99,3 +99,15 @@ def test_product_sources_do_not_reach_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "oracle/" not in text and "liboracle" not in text, f
+
+
+def test_static_scratch_limits_on_the_host(moe):
+    """The entry point without a workspace refuses sizes whose scratch exceeds its
+    32 MiB array, and invalid sizes, before any CUDA call; the decode shapes fit."""
+    L = moe.lib()
+    nul = [None] * 9
+    assert L.moe_forward_static_scratch(*nul, 8192, 2880, 2880, 128, 4, None, None) == 3  # MOE_ERR_WORKSPACE
+    assert L.moe_forward_static_scratch(*nul, 0, 2880, 2880, 128, 4, None, None) == 1  # MOE_ERR_INVALID_ARG
+    for T, E in ((64, 32), (256, 128)):
+        assert 0 < L.moe_workspace_size(T, 2880, 2880, E, 4) <= (32 << 20)
+    assert L.moe_workspace_size(8192, 2880, 2880, 128, 4) > (32 << 20)
