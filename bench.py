@@ -4,9 +4,10 @@
 One step = one call of the whole layer (router, top-k + softmax, grouping by
 expert + FP8 quantisation of x, gate/up GEMM + SwiGLU + requant, down GEMM +
 routing-weight scale, combine) over one batch of T synthetic tokens whose
-inputs are resident in HBM.  L2 is flushed (256 MiB write) before every step
-and the step is timed with CUDA events on the launching stream; the flush is
-outside the events.
+inputs are resident in HBM.  L2 is flushed before every step (a 256 MiB write,
+then a 256 MiB read, so that the step neither finds its inputs in L2 nor has to
+write back the flush's dirty lines) and the step is timed with CUDA events on
+the launching stream; the flush is outside the events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
                   [--format block128|mx|mxfp4]
@@ -278,6 +279,15 @@ def cpu_oracle_leg(cfg, seconds: float, mx: bool = False, fp4: bool = False):
     return passes * n / dt, desc, dt
 
 
+def flush_l2(wbuf, rbuf, i: int) -> None:
+    """Leave L2 cold and clean before a timed step: writing `wbuf` (larger than
+    L2) evicts whatever the previous step left there, and reading `rbuf` (also
+    larger than L2) then evicts the dirty lines of that write, so their
+    write-back happens here instead of inside the step's first kernels."""
+    wbuf.fill_(i & 0xFF)
+    rbuf.sum()
+
+
 def max_over_ranks(ms: float, pg, device) -> float:
     """The slowest rank's time (every rank receives it); the value itself on one rank."""
     if pg is None:
@@ -385,10 +395,11 @@ def main():
     T, H = cfg.T, cfg.H
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.zeros(FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush_l2(flush, flush_rd, 1)
         layer(x_dev, out=out)
     torch.cuda.synchronize()
     ws = layer.workspace(T)
@@ -404,7 +415,7 @@ def main():
         moe.forward(x_dev, layer.router_w, layer.router_b, layer.w13, layer.s13, layer.b13, layer.w2, layer.s2,
                     layer.b2, cfg.top_k, out=out, workspace=ws)
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush_l2(flush, flush_rd, 1)
         graph.replay()
     torch.cuda.synchronize()
     ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -420,7 +431,7 @@ def main():
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for i in range(K):
-        flush.fill_(i & 0xFF)
+        flush_l2(flush, flush_rd, i)
         ev_s[i].record(stream)
         graph.replay()
         ev_e[i].record(stream)
@@ -439,7 +450,7 @@ def main():
             e.record(stream)
     torch.cuda.synchronize()
     for i in range(K):
-        flush.fill_(i & 0xFF)
+        flush_l2(flush, flush_rd, i)
         # a ~0.1 ms spin kernel lets the host enqueue the whole step before its
         # first event, so no stage time contains host launch latency
         torch.cuda._sleep(200_000)
@@ -463,7 +474,7 @@ def main():
         out_host.copy_(glayer(), non_blocking=True)
     torch.cuda.synchronize()
     for i in range(K):
-        flush.fill_(i & 0xFF)
+        flush_l2(flush, flush_rd, i)
         e2e_ev[i][0].record(stream)
         glayer.x.copy_(x_host, non_blocking=True)
         out_host.copy_(glayer(), non_blocking=True)
@@ -510,7 +521,8 @@ def main():
                 config=dict(workload=workload_str(cfg) + ("" if args.routing == "synthetic" else
                                                           " routing=one row per expert (T = E/top_k)"),
                             parallelism=f"replicas{world}",
-                            l2="flushed before every step (256 MiB write, outside the timed events)",
+                            l2="flushed before every step (256 MiB write, then 256 MiB read so no dirty line is left; "
+                               "outside the timed events)",
                             weights=WEIGHTS[args.format]),
                 roofline=roof,
                 step=dict(ms_per_stage=stage_ms, active_experts=alg["active"],

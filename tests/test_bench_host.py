@@ -81,3 +81,12 @@ def test_prefill_flops_of_the_stated_workloads():
     cfg = synth.config("qwen235b_prefill")
     a = bench.algorithmic(cfg, np.full(cfg.E, cfg.T * cfg.top_k // cfg.E))
     assert a["gemm1_flops"] + a["gemm2_flops"] == pytest.approx(4.948e12, rel=1e-3)
+
+
+def test_flush_writes_one_buffer_and_reads_the_other():
+    import torch
+    w = torch.zeros(1 << 12, dtype=torch.uint8)
+    r = torch.zeros(1 << 9, dtype=torch.int64)
+    bench.flush_l2(w, r, 0x1A5)
+    assert int(w.min()) == int(w.max()) == 0xA5  # the step index's low byte, every byte written
+    assert int(r.abs().sum()) == 0  # the read buffer is only read
