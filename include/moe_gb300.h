@@ -30,9 +30,12 @@
  *   contiguous HBM read.  moe_pack_weights builds this layout.
  *
  * Ownership: the caller owns every buffer, including the workspace.  Calls
- * never allocate device memory, never synchronise the stream (except
- * moe_read_device_status), keep no data between calls and are asynchronous
- * on `stream`.  Inputs are read-only; `out` is fully overwritten.
+ * never allocate device memory, never synchronise the stream (except the two
+ * status readers), keep no data between calls and are asynchronous on
+ * `stream`.  Inputs are read-only; `out` is fully overwritten.  One exception:
+ * moe_forward_static_scratch (below) uses a device array inside the library
+ * instead of a workspace; that array lives until the process exits and keeps
+ * the last call's contents.
  *
  * Errors: arguments are checked before any launch (MOE_ERR_INVALID_ARG,
  * MOE_ERR_UNSUPPORTED for pointers that are not 16-byte aligned or sizes
@@ -132,21 +135,65 @@ moe_status moe_forward_profiled(const void* x, const void* router_w, const void*
  * and results as moe_forward, without the workspace: the library uses a
  * file-scope device array of 32 MiB (MOE_STATIC_SCRATCH_BYTES) instead, which
  * every GPU that loads the library holds until the process exits.
- *   - Sizes whose moe_workspace_size exceeds 32 MiB are rejected with
- *     MOE_ERR_WORKSPACE before anything is launched.
- *   - The first call on a device, with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress); make that first call
- *     before any stream capture.
+ *   - Null pointers and invalid sizes return MOE_ERR_INVALID_ARG; sizes whose
+ *     moe_workspace_size exceeds 32 MiB are rejected with MOE_ERR_WORKSPACE,
+ *     both before anything is launched.
+ *   - The first call in a CUDA context (per device, with that device current)
+ *     looks up the array's device address (cudaGetSymbolAddress); make that
+ *     first call before any stream capture.  A new context on the device (for
+ *     example after cudaDeviceReset) is noticed and the address looked up
+ *     again on the next call.
  *   - Every call on a device shares the one array and it keeps the last
  *     call's contents (each call clears what must start at zero itself).
  *     Calls whose kernels overlap on the GPU (other streams, other host
  *     threads) race on it; serialise them.
+ *   - A device wait that ran out is reported by moe_read_static_scratch_status,
+ *     not by the call's return value; the next call clears it.
  *   - Calls no cudaMalloc, cudaFree or allocating library routine.
  */
 #define MOE_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 moe_status moe_forward_static_scratch(const void* x, const void* router_w, const void* router_b, const uint8_t* w13,
                                       const float* s13, const void* b13, const uint8_t* w2, const float* s2,
                                       const void* b2, int T, int H, int I, int E, int top_k, void* out, void* stream);
+
+/* moe_read_device_status for the array of moe_forward_static_scratch on the
+ * current device: synchronises `stream`, then reads and clears the error word
+ * the last call left there (MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_CUDA). */
+moe_status moe_read_static_scratch_status(void* stream);
+
+/*
+ * Routing steps alone, into caller buffers ("GPT-OSS on Day 0", MoE section:
+ * the routing kernel -- top-k, then softmax over the selected experts -- kept
+ * separate from the expert GEMMs, whose inputs it groups by expert):
+ *   topk_idx int32 [T, top_k]  selected experts, ascending, ties -> lower index
+ *   topk_w   fp32  [T, top_k]  softmax over the k logits before bf16 rounding
+ *   offset   int32 [E+1]       first permuted row of each expert
+ *   perm     int32 [R]         row r -> t*top_k + j, rows sorted by (expert, token)
+ *   xq       e4m3  [R, Hp]     1x128 FP8 codes of x in permuted rows (pad codes 0)
+ *   sx       fp32  [Hp/128, R] their group scales, K-block-major (sx[g*R + r])
+ * The same kernels as moe_forward's first two stages.  x, router_w and xq must
+ * be 16-byte aligned, the workspace (moe_route_workspace_size bytes) 256-byte
+ * aligned; errors as moe_forward.  Asynchronous on `stream`.
+ */
+size_t moe_route_workspace_size(int T, int H, int E, int top_k);
+moe_status moe_route_debug(const void* x, const void* router_w, const void* router_b, int T, int H, int E, int top_k,
+                           int32_t* topk_idx, float* topk_w, int32_t* offset, int32_t* perm, uint8_t* xq, float* sx,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Row-major FP8 weight codes -> the blocked layout the forward reads.  The
+ * layer's weights are e4m3 codes with 128x128 block scales ("GPT-OSS on Day
+ * 0", infrastructure decisions); a caller that holds them row-major,
+ *   w13_rm [E, 2*Ip, Hp] (gate rows [0, I), up rows [Ip, Ip+I), zero padding)
+ *   w2_rm  [E, Hp, Ip]
+ * gets w13 [E, 2*Ip/128, Hp/128, 128, 128] and w2 [E, Hp/128, Ip/128, 128,
+ * 128] (each 128x128 block 16 KB contiguous).  The block scales s13 / s2 are
+ * the same in both layouts and are not touched.  Also valid for MXFP8 codes
+ * (same code layout).  All pointers 16-byte aligned device pointers; either
+ * pair may be NULL to convert only the other.  Asynchronous on `stream`.
+ */
+moe_status moe_block_weights(const uint8_t* w13_rm, const uint8_t* w2_rm, int H, int I, int E, uint8_t* w13,
+                             uint8_t* w2, void* stream);
 
 /*
  * Weight packer (the offline converter from master weights to the layer's
@@ -165,7 +212,13 @@ moe_status moe_pack_weights(const float* w13_f32, const float* w2_f32, int H, in
  * The 1x128 group quantiser on its own (the step the gate/up GEMM epilogue
  * applies to h, and the one applied to x): in fp32 [rows, cols] with row
  * stride ld_in (elements) -> q e4m3 [rows, ceil(cols/128)*128],
- * s fp32 [rows, ceil(cols/128)].  Same device arithmetic as the fused epilogue.
+ * s fp32 [rows, ceil(cols/128)].  It shares the per-value steps with the
+ * fused epilogues -- the scale amax/448, its reciprocal, the corrected
+ * quotient (IEEE division for groups with 0 < amax < 2^-64) and the e4m3
+ * conversion -- but not the way they find a group's amax: the decode
+ * epilogue takes a column maximum across a warp and switches the whole warp
+ * to IEEE division when any of its tokens needs it, and the prefill epilogue
+ * joins two warps' partial maxima through shared memory.
  */
 moe_status moe_quantize_rows(const float* in, int rows, int cols, int ld_in, uint8_t* q, float* s, void* stream);
 

@@ -20,7 +20,7 @@ __all__ = ["MoeError", "build", "lib", "workspace_size", "workspace_layout", "wo
            "read_device_status", "test_bounded_wait", "MoeLayer", "pad128", "pack_weights_mx",
            "pack_weights_into_mx", "s13_mx_shape", "s2_mx_shape", "unblock_scales_mx", "quantize_rows_mx",
            "pack_weights_mxfp4", "pack_weights_into_mxfp4", "w13_shape_fp4", "w2_shape_fp4", "unblock_fp4",
-           "weight_format"]
+           "weight_format", "route_debug", "block_weights", "read_static_scratch_status"]
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "CUDA error",
           5: "device wait timed out"}
@@ -61,6 +61,14 @@ def lib():
         L.moe_forward_profiled.restype = i32
         L.moe_forward_static_scratch.argtypes = [vp] * 9 + [i32] * 5 + [vp, vp]
         L.moe_forward_static_scratch.restype = i32
+        L.moe_read_static_scratch_status.argtypes = [vp]
+        L.moe_read_static_scratch_status.restype = i32
+        L.moe_route_workspace_size.argtypes = [i32] * 4
+        L.moe_route_workspace_size.restype = sz
+        L.moe_route_debug.argtypes = [vp] * 3 + [i32] * 4 + [vp] * 7 + [sz, vp]
+        L.moe_route_debug.restype = i32
+        L.moe_block_weights.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
+        L.moe_block_weights.restype = i32
         L.moe_pack_weights.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
         L.moe_pack_weights.restype = i32
         L.moe_quantize_rows.argtypes = [vp, i32, i32, i32, vp, vp, vp]
@@ -391,6 +399,54 @@ def quantize_rows(v: torch.Tensor, stream=None):
     _check(lib().moe_quantize_rows(_dev(v, torch.float32, "v"), rows, cols, cols, q.data_ptr(), s.data_ptr(),
                                    _stream(stream)), "moe_quantize_rows")
     return q, s
+
+
+def route_debug(x, router_w, router_b, top_k: int, stream=None) -> dict:
+    """The routing steps alone (moe_route_debug): topk_idx [T, k] int32, topk_w [T, k]
+    fp32, offset [E+1], perm [R], xq [R, Hp] e4m3 codes and sx [R, Hp/128] (stored
+    K-block-major, returned transposed as a view) in new device tensors."""
+    T, H = x.shape
+    E = router_w.shape[0]
+    R, Hp = T * top_k, pad128(H)
+    dev = x.device
+    need = int(lib().moe_route_workspace_size(T, H, E, top_k))
+    if need == 0:
+        raise MoeError(1, "moe_route_workspace_size")
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    o = dict(topk_idx=torch.empty((T, top_k), dtype=torch.int32, device=dev),
+             topk_w=torch.empty((T, top_k), dtype=torch.float32, device=dev),
+             offset=torch.empty(E + 1, dtype=torch.int32, device=dev),
+             perm=torch.empty(R, dtype=torch.int32, device=dev),
+             xq=torch.empty((R, Hp), dtype=torch.uint8, device=dev),
+             sx_kmajor=torch.empty((Hp // 128, R), dtype=torch.float32, device=dev))
+    code = lib().moe_route_debug(_dev(x, torch.bfloat16, "x"), _dev(router_w, torch.bfloat16, "router_w"),
+                                 _dev(router_b, torch.bfloat16, "router_b"), T, H, E, top_k, o["topk_idx"].data_ptr(),
+                                 o["topk_w"].data_ptr(), o["offset"].data_ptr(), o["perm"].data_ptr(),
+                                 o["xq"].data_ptr(), o["sx_kmajor"].data_ptr(), ws.data_ptr(), ws.numel(),
+                                 _stream(stream))
+    _check(code, "moe_route_debug")
+    o["sx"] = o["sx_kmajor"].t()
+    return o
+
+
+def block_weights(w13_rm: torch.Tensor, w2_rm: torch.Tensor, H: int, I: int, stream=None):
+    """Row-major e4m3 codes w13 [E, 2*Ip, Hp], w2 [E, Hp, Ip] (uint8) -> the blocked
+    layout of w13_shape / w2_shape (moe_block_weights)."""
+    E = w13_rm.shape[0]
+    Hp, Ip = pad128(H), pad128(I)
+    if tuple(w13_rm.shape) != (E, 2 * Ip, Hp) or tuple(w2_rm.shape) != (E, Hp, Ip):
+        raise ValueError("row-major code shapes do not match H, I")
+    q13 = torch.empty(w13_shape(E, H, I), dtype=torch.uint8, device=w13_rm.device)
+    q2 = torch.empty(w2_shape(E, H, I), dtype=torch.uint8, device=w13_rm.device)
+    _check(lib().moe_block_weights(_dev(w13_rm, torch.uint8, "w13_rm"), _dev(w2_rm, torch.uint8, "w2_rm"), H, I, E,
+                                   q13.data_ptr(), q2.data_ptr(), _stream(stream)), "moe_block_weights")
+    return q13, q2
+
+
+def read_static_scratch_status(stream=None) -> int:
+    """Synchronise and return the device status code moe_forward_static_scratch
+    left in its array on the current device (0 = ok, 5 = a wait timed out)."""
+    return int(lib().moe_read_static_scratch_status(_stream(stream)))
 
 
 def read_device_status(workspace: torch.Tensor, stream=None) -> int:

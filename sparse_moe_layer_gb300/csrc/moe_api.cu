@@ -144,6 +144,105 @@ enum WeightFormat { kBlock128 = 0, kMxfp8 = 1, kMxfp4 = 2 };
 
 }  // namespace
 
+// What the router and the permutation kernel write (device pointers).
+struct RoutingBuffers {
+    uint32_t* status;     // uint32[64], zeroed here
+    int32_t* hist;        // [ceil(T/256), E] + 1 arrival counter, zeroed here (directly after status)
+    int32_t* count;       // [E]
+    int32_t* offset;      // [E+1]
+    int32_t* chunk_base;  // [ceil(T/256), E]
+    int32_t* tiles1;      // [E+1]
+    int32_t* tiles2;      // [E+1]
+    int32_t* topk_idx;    // [T, k]
+    float* topk_w;        // [T, k]
+    uint16_t* topk_wb;    // [T, k]
+    int32_t* perm;        // [R]
+    int32_t* inv;         // [R]
+    uint8_t* xq;          // [R, Hp]
+    float* sx;            // [Hp/128, R] (MXFP8: scale atoms)
+};
+
+// Steps a1-a4 on `st`: the status words and the histogram cleared, the router
+// (top-k, softmax, per-chunk expert histogram), then the permutation with the
+// x quantisation (1x128, or 1x32 MX when mx).  bm, nt1, nt2 size the GEMM tile
+// lists the scan writes.  `mid` (optional) is recorded between the two kernels.
+static moe_status launch_routing(const void* x, const void* router_w, const void* router_b, int T, int H, int E,
+                                 int top_k, int bm, int nt1, int nt2, bool mx, const RoutingBuffers& b,
+                                 cudaStream_t st, cudaEvent_t mid) {
+    const int Hp = pad128(H);
+    const int nch = (T + kChunkTokens - 1) / kChunkTokens;
+    // status words and the (chunk, expert) histogram with its arrival counter start at zero
+    const size_t zero_bytes = reinterpret_cast<uint8_t*>(b.hist + (size_t)nch * E + 1) -
+                              reinterpret_cast<uint8_t*>(b.status);
+    if (cudaMemsetAsync(b.status, 0, zero_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+    RouteParams rp;
+    rp.x = static_cast<const uint16_t*>(x);
+    rp.rw = static_cast<const uint16_t*>(router_w);
+    rp.rb = static_cast<const uint16_t*>(router_b);
+    rp.T = T;
+    rp.H = H;
+    rp.E = E;
+    rp.k = top_k;
+    rp.nchunks = nch;
+    rp.bm = bm;
+    rp.nt1 = nt1;
+    rp.nt2 = nt2;
+    rp.topk_idx = b.topk_idx;
+    rp.topk_w = b.topk_w;
+    rp.topk_wb = b.topk_wb;
+    rp.hist = b.hist;
+    rp.done = b.hist + (size_t)nch * E;
+    rp.scan_in_router = router_scans(T) ? 1 : 0;
+    rp.count = b.count;
+    rp.offset = b.offset;
+    rp.chunk_base = b.chunk_base;
+    rp.tiles1 = b.tiles1;
+    rp.tiles2 = b.tiles2;
+    rp.status = b.status;
+    // large batches with 16-byte aligned rows: the tensor-core router
+    if (const int np = router_tc_experts(T, H, E)) {
+        CUtensorMap tmX, tmW;
+        if (!make_map_bf16(&tmX, x, T, H, 128) || !make_map_bf16(&tmW, router_w, E, H, (uint32_t)np))
+            return MOE_ERR_CUDA;
+        if (launch_router_tc(rp, tmX, tmW, st) != cudaSuccess) return MOE_ERR_CUDA;
+    } else if (launch_router(rp, st) != cudaSuccess) {
+        return MOE_ERR_CUDA;
+    }
+    if (mid) cudaEventRecord(mid, st);
+
+    PermuteParams pp;
+    pp.x = rp.x;
+    pp.T = T;
+    pp.H = H;
+    pp.Hp = Hp;
+    pp.E = E;
+    pp.k = top_k;
+    // 8 tokens per CTA for large batches while their x rows fit in 96 KB of shared memory
+    pp.tokens_per_cta = (T > 2048 && 8LL * ((H + 7) & ~7) * 2 <= 96 * 1024) ? 8 : 1;
+    pp.topk_idx = b.topk_idx;
+    pp.chunk_base = b.chunk_base;
+    pp.scan_here = router_scans(T) ? 0 : 1;
+    pp.nchunks = nch;
+    pp.bm = bm;
+    pp.nt1 = nt1;
+    pp.nt2 = nt2;
+    pp.hist = b.hist;
+    pp.count = b.count;
+    pp.offset = b.offset;
+    pp.tiles1 = b.tiles1;
+    pp.tiles2 = b.tiles2;
+    pp.status = b.status;
+    pp.perm = b.perm;
+    pp.inv = b.inv;
+    pp.xq = b.xq;
+    pp.R = T * top_k;
+    pp.sx = b.sx;
+    pp.mx = mx ? 1 : 0;
+    pp.sxa = reinterpret_cast<uint8_t*>(b.sx);
+    if (launch_permute_quant(pp, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
 // Launch sequence shared by moe_forward and moe_forward_profiled; when `ev`
 // is non-null, ev[i] is recorded on the stream before stage i and ev[5]
 // after the last stage.
@@ -264,95 +363,50 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const int Hp = pad128(H), Ip = pad128(I);
     const int R = T * top_k;
-    const int nch = (T + kChunkTokens - 1) / kChunkTokens;
     const int sms = num_sms();
 
-    // status words and the (chunk, expert) histogram start at zero
     mark(0);
-    if (cudaMemsetAsync(ws, 0, L.count, st) != cudaSuccess) return MOE_ERR_CUDA;
 
-    RouteParams rp;
-    rp.x = static_cast<const uint16_t*>(x);
-    rp.rw = static_cast<const uint16_t*>(router_w);
-    rp.rb = static_cast<const uint16_t*>(router_b);
-    rp.T = T;
-    rp.H = H;
-    rp.E = E;
-    rp.k = top_k;
-    rp.nchunks = nch;
     // Few rows per expert (decode): weight-streaming kernels with 32-row token
     // tiles and 128-feature n-tiles; else 128-row tiles of 128 h features
     // (gate/up) or 256 output features (down: two w2 blocks per tile).
     const bool decode = decode_sized(R, E);
-    rp.bm = decode ? 32 : 128;
-    rp.nt1 = Ip / 128;
-    rp.nt2 = decode ? Hp / 128 : (Hp / 128 + 1) / 2;
-    rp.topk_idx = reinterpret_cast<int32_t*>(ws + L.topk_idx);
-    rp.topk_w = reinterpret_cast<float*>(ws + L.topk_w);
-    rp.topk_wb = reinterpret_cast<uint16_t*>(ws + L.topk_wb);
-    rp.hist = reinterpret_cast<int32_t*>(ws + L.hist);
-    rp.done = rp.hist + (size_t)nch * E;
-    rp.scan_in_router = router_scans(T) ? 1 : 0;
-    rp.count = reinterpret_cast<int32_t*>(ws + L.count);
-    rp.offset = reinterpret_cast<int32_t*>(ws + L.offset);
-    rp.chunk_base = reinterpret_cast<int32_t*>(ws + L.chunk_base);
-    rp.tiles1 = reinterpret_cast<int32_t*>(ws + L.tiles1);
-    rp.tiles2 = reinterpret_cast<int32_t*>(ws + L.tiles2);
-    rp.status = reinterpret_cast<uint32_t*>(ws + L.status);
-    // large batches with 16-byte aligned rows: the tensor-core router
-    if (const int np = router_tc_experts(T, H, E)) {
-        CUtensorMap tmX, tmW;
-        if (!make_map_bf16(&tmX, x, T, H, 128) || !make_map_bf16(&tmW, router_w, E, H, (uint32_t)np))
-            return MOE_ERR_CUDA;
-        if (launch_router_tc(rp, tmX, tmW, st) != cudaSuccess) return MOE_ERR_CUDA;
-    } else if (launch_router(rp, st) != cudaSuccess) {
-        return MOE_ERR_CUDA;
+    const int bm = decode ? 32 : 128;
+    const int nt1 = Ip / 128;
+    const int nt2 = decode ? Hp / 128 : (Hp / 128 + 1) / 2;
+    RoutingBuffers rb;
+    rb.status = reinterpret_cast<uint32_t*>(ws + L.status);
+    rb.hist = reinterpret_cast<int32_t*>(ws + L.hist);
+    rb.count = reinterpret_cast<int32_t*>(ws + L.count);
+    rb.offset = reinterpret_cast<int32_t*>(ws + L.offset);
+    rb.chunk_base = reinterpret_cast<int32_t*>(ws + L.chunk_base);
+    rb.tiles1 = reinterpret_cast<int32_t*>(ws + L.tiles1);
+    rb.tiles2 = reinterpret_cast<int32_t*>(ws + L.tiles2);
+    rb.topk_idx = reinterpret_cast<int32_t*>(ws + L.topk_idx);
+    rb.topk_w = reinterpret_cast<float*>(ws + L.topk_w);
+    rb.topk_wb = reinterpret_cast<uint16_t*>(ws + L.topk_wb);
+    rb.perm = reinterpret_cast<int32_t*>(ws + L.perm);
+    rb.inv = reinterpret_cast<int32_t*>(ws + L.inv);
+    rb.xq = ws + L.xq;
+    rb.sx = reinterpret_cast<float*>(ws + L.sx);
+    {
+        const moe_status rs = launch_routing(x, router_w, router_b, T, H, E, top_k, bm, nt1, nt2, mx, rb, st,
+                                             ev ? static_cast<cudaEvent_t>(ev[1]) : nullptr);
+        if (rs != MOE_OK) return rs;
     }
-    mark(1);
-
-    PermuteParams pp;
-    pp.x = rp.x;
-    pp.T = T;
-    pp.H = H;
-    pp.Hp = Hp;
-    pp.E = E;
-    pp.k = top_k;
-    // 8 tokens per CTA for large batches while their x rows fit in 96 KB of shared memory
-    pp.tokens_per_cta = (T > 2048 && 8LL * ((H + 7) & ~7) * 2 <= 96 * 1024) ? 8 : 1;
-    pp.topk_idx = rp.topk_idx;
-    pp.chunk_base = rp.chunk_base;
-    pp.scan_here = router_scans(T) ? 0 : 1;
-    pp.nchunks = nch;
-    pp.bm = rp.bm;
-    pp.nt1 = rp.nt1;
-    pp.nt2 = rp.nt2;
-    pp.hist = rp.hist;
-    pp.count = rp.count;
-    pp.offset = rp.offset;
-    pp.tiles1 = rp.tiles1;
-    pp.tiles2 = rp.tiles2;
-    pp.status = rp.status;
-    pp.perm = reinterpret_cast<int32_t*>(ws + L.perm);
-    pp.inv = reinterpret_cast<int32_t*>(ws + L.inv);
-    pp.xq = ws + L.xq;
-    pp.R = R;
-    pp.sx = reinterpret_cast<float*>(ws + L.sx);
-    pp.mx = mx ? 1 : 0;
-    pp.sxa = ws + L.sx;
-    if (launch_permute_quant(pp, st) != cudaSuccess) return MOE_ERR_CUDA;
     mark(2);
 
     // upper bound of the tile count of either GEMM: sum_e ceil(count_e/bm) <= E + R/bm
-    const long long mt_bound = (long long)E + (R + rp.bm - 1) / rp.bm;
+    const long long mt_bound = (long long)E + (R + bm - 1) / bm;
 
     CUtensorMap tmA1, tmB1, tmA2, tmB2;
     // weights are blocked: a 2D view of 128-byte rows, one 128x128 block = 128 consecutive rows
     // decode kernels load a tile's activation rows in boxes of kDecXBoxRows, only as many as it has rows
-    const uint32_t a_box = decode ? kDecXBoxRows : (uint32_t)rp.bm;
+    const uint32_t a_box = decode ? kDecXBoxRows : (uint32_t)bm;
     const uint64_t rows13 = (uint64_t)E * 2 * Ip * (Hp / 128), rows2 = (uint64_t)E * Hp * (Ip / 128);
     const bool wmaps = fmt == kMxfp4 ? make_map_fp4(&tmB1, w13, rows13) && make_map_fp4(&tmB2, w2, rows2)
                                      : make_map(&tmB1, w13, rows13, 128) && make_map(&tmB2, w2, rows2, 128);
-    if (!wmaps || !make_map(&tmA1, pp.xq, R, Hp, a_box) || !make_map(&tmA2, ws + L.hq, R, Ip, a_box))
+    if (!wmaps || !make_map(&tmA1, rb.xq, R, Hp, a_box) || !make_map(&tmA2, ws + L.hq, R, Ip, a_box))
         return MOE_ERR_CUDA;
 
     if (mx) {
@@ -364,18 +418,18 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
         m1.N_real = I;
         m1.sw_rowblocks = 2 * Ip / 128;
         m1.up_rows = Ip;
-        m1.nt = rp.nt1;
-        m1.count = rp.count;
-        m1.offset = rp.offset;
-        m1.tiles = rp.tiles1;
+        m1.nt = nt1;
+        m1.count = rb.count;
+        m1.offset = rb.offset;
+        m1.tiles = rb.tiles1;
         m1.sa = ws + L.sx;
         m1.sw = static_cast<const uint8_t*>(s13);
         m1.bias = static_cast<const uint16_t*>(b13);
         m1.hq = ws + L.hq;
         m1.sh = ws + L.sh;
         m1.ldq = Ip;
-        m1.status = rp.status;
-        const long long t1 = mt_bound * rp.nt1;
+        m1.status = rb.status;
+        const long long t1 = mt_bound * nt1;
         if (launch_gemm_mx(true, decode, fmt == kMxfp4, tmA1, tmB1, m1, (int)(t1 < sms ? t1 : sms), st) != cudaSuccess)
             return MOE_ERR_CUDA;
         mark(3);
@@ -386,19 +440,19 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
         m2.KB = Ip / 128;
         m2.N_real = H;
         m2.sw_rowblocks = Hp / 128;
-        m2.nt = rp.nt2;
-        m2.count = rp.count;
-        m2.offset = rp.offset;
-        m2.tiles = rp.tiles2;
+        m2.nt = nt2;
+        m2.count = rb.count;
+        m2.offset = rb.offset;
+        m2.tiles = rb.tiles2;
         m2.sa = ws + L.sh;
         m2.sw = static_cast<const uint8_t*>(s2);
         m2.bias = static_cast<const uint16_t*>(b2);
-        m2.perm = pp.perm;
-        m2.topk_wb = rp.topk_wb;
+        m2.perm = rb.perm;
+        m2.topk_wb = rb.topk_wb;
         m2.part = reinterpret_cast<float*>(ws + L.part);
         m2.ldp = Hp;
-        m2.status = rp.status;
-        const long long t2 = mt_bound * rp.nt2;
+        m2.status = rb.status;
+        const long long t2 = mt_bound * nt2;
         if (launch_gemm_mx(false, decode, fmt == kMxfp4, tmA2, tmB2, m2, (int)(t2 < sms ? t2 : sms), st) != cudaSuccess)
             return MOE_ERR_CUDA;
         mark(4);
@@ -417,16 +471,16 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     g1.rows_B = 2 * Ip;
     g1.up_rows = Ip;
     g1.sw_rowblocks = 2 * Ip / 128;
-    g1.count = rp.count;
-    g1.offset = rp.offset;
-    g1.tiles = rp.tiles1;
-    g1.sa = pp.sx;
+    g1.count = rb.count;
+    g1.offset = rb.offset;
+    g1.tiles = rb.tiles1;
+    g1.sa = rb.sx;
     g1.sw = static_cast<const float*>(s13);
     g1.bias = static_cast<const uint16_t*>(b13);
     g1.hq = ws + L.hq;
     g1.sh = reinterpret_cast<float*>(ws + L.sh);
     g1.ldq = Ip;
-    g1.status = rp.status;
+    g1.status = rb.status;
     long long t1 = mt_bound * (Ip / 128);
     int grid1 = (int)(t1 < sms ? t1 : sms);
     if ((decode ? launch_gemm_gateup_decode(tmB1, tmA1, g1, grid1, st) : launch_gemm_gateup(tmA1, tmB1, g1, grid1, st))
@@ -443,18 +497,18 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     g2.rows_B = Hp;
     g2.up_rows = 0;
     g2.sw_rowblocks = Hp / 128;
-    g2.count = rp.count;
-    g2.offset = rp.offset;
-    g2.tiles = rp.tiles2;
+    g2.count = rb.count;
+    g2.offset = rb.offset;
+    g2.tiles = rb.tiles2;
     g2.sa = g1.sh;
     g2.sw = static_cast<const float*>(s2);
     g2.bias = static_cast<const uint16_t*>(b2);
-    g2.perm = pp.perm;
-    g2.topk_wb = rp.topk_wb;
+    g2.perm = rb.perm;
+    g2.topk_wb = rb.topk_wb;
     g2.part = reinterpret_cast<float*>(ws + L.part);
     g2.ldp = Hp;
-    g2.status = rp.status;
-    long long t2 = mt_bound * rp.nt2;
+    g2.status = rb.status;
+    long long t2 = mt_bound * nt2;
     int grid2 = (int)(t2 < sms ? t2 : sms);
     if ((decode ? launch_gemm_down_decode(tmB2, tmA2, g2, grid2, st) : launch_gemm_down(tmA2, tmB2, g2, grid2, st)) !=
         cudaSuccess)
@@ -485,34 +539,159 @@ __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+// Per device: the context the address was looked up in, and the address.  A
+// context torn down and made again (cudaDeviceReset, or the primary context
+// released and retained anew) loads the module again, possibly elsewhere, so
+// the address is looked up again whenever the current context differs.
+struct ScratchAddr {
+    CUcontext ctx;
+    void* ptr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
+
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+std::once_flag g_ctx_once;
+
+CUcontext current_context() {
+    std::call_once(g_ctx_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    });
+    CUcontext c = nullptr;
+    if (!g_ctx_current || g_ctx_current(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
+// Device address of g_static_scratch on the current device, looked up with
+// cudaGetSymbolAddress the first time in each context (that first lookup may
+// load the module, so it must not happen inside a stream capture).
+moe_status static_scratch_address(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    ScratchAddr& a = g_scratch_addr[dev];
+    const CUcontext now = current_context();
+    if (!a.ptr || !now || a.ctx != now) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+        a.ptr = p;
+        a.ctx = current_context();  // the lookup above made the context current if none was
+    }
+    *out = a.ptr;
+    return MOE_OK;
+}
 }  // namespace
 
 extern "C" moe_status moe_forward_static_scratch(const void* x, const void* router_w, const void* router_b,
                                                  const uint8_t* w13, const float* s13, const void* b13,
                                                  const uint8_t* w2, const float* s2, const void* b2, int T, int H,
                                                  int I, int E, int top_k, void* out, void* stream) {
+    // argument errors first, then the size limit of the static array
+    if (!x || !router_w || !router_b || !w13 || !s13 || !b13 || !w2 || !s2 || !b2 || !out) return MOE_ERR_INVALID_ARG;
     const size_t need = moe_workspace_size(T, H, I, E, top_k);
     if (need == 0) return MOE_ERR_INVALID_ARG;
     if (need > kStaticScratchBytes) return MOE_ERR_WORKSPACE;  // these sizes need more than the static area
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
     void* scratch = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_scratch_mu);
-        if (!g_scratch_addr[dev]) {
-            // first call on this device (which is current): find the array's device address
-            void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
-            g_scratch_addr[dev] = p;
-        }
-        scratch = g_scratch_addr[dev];
-    }
+    const moe_status st = static_scratch_address(&scratch);
+    if (st != MOE_OK) return st;
     // forward_impl clears the status words and the expert histogram at the
     // start of every call, so nothing left by the previous call leaks in.
     return forward_impl(x, router_w, router_b, w13, s13, b13, w2, s2, b2, T, H, I, E, top_k, out, scratch,
                         kStaticScratchBytes, stream, nullptr);
+}
+
+// The device error word of the static array (its first word, as in a
+// caller's workspace): read after synchronising the stream, then cleared.
+extern "C" moe_status moe_read_static_scratch_status(void* stream) {
+    void* scratch = nullptr;
+    const moe_status st = static_scratch_address(&scratch);
+    if (st != MOE_OK) return st;
+    return moe_read_device_status(scratch, stream);
+}
+
+// Workspace of moe_route_debug: the intermediates of the routing steps that
+// the caller does not ask for, carved like the forward's workspace.
+namespace {
+struct RouteLayout {
+    size_t status, hist, count, chunk_base, tiles1, tiles2, topk_wb, inv, total;
+};
+RouteLayout route_layout_of(int T, int E, int k) {
+    const size_t R = (size_t)T * k;
+    const size_t nch = (T + kChunkTokens - 1) / kChunkTokens;
+    RouteLayout L;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L.status = take(kStatusWords * 4);
+    L.hist = take((nch * E + 1) * 4);
+    L.count = take((size_t)E * 4);
+    L.chunk_base = take(nch * E * 4);
+    L.tiles1 = take((size_t)(E + 1) * 4);
+    L.tiles2 = take((size_t)(E + 1) * 4);
+    L.topk_wb = take(R * 2);
+    L.inv = take(R * 4);
+    L.total = o;
+    return L;
+}
+}  // namespace
+
+extern "C" size_t moe_route_workspace_size(int T, int H, int E, int top_k) {
+    if (!sizes_ok(T, H, 1, E, top_k)) return 0;
+    return route_layout_of(T, E, top_k).total;
+}
+
+extern "C" moe_status moe_route_debug(const void* x, const void* router_w, const void* router_b, int T, int H, int E,
+                                      int top_k, int32_t* topk_idx, float* topk_w, int32_t* offset, int32_t* perm,
+                                      uint8_t* xq, float* sx, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+    if (!x || !router_w || !router_b || !topk_idx || !topk_w || !offset || !perm || !xq || !sx || !workspace)
+        return MOE_ERR_INVALID_ARG;
+    if (!sizes_ok(T, H, 1, E, top_k)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(router_w) || !aligned16(xq) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MOE_ERR_UNSUPPORTED;
+    const RouteLayout L = route_layout_of(T, E, top_k);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    RoutingBuffers b;
+    b.status = reinterpret_cast<uint32_t*>(ws + L.status);
+    b.hist = reinterpret_cast<int32_t*>(ws + L.hist);
+    b.count = reinterpret_cast<int32_t*>(ws + L.count);
+    b.offset = offset;
+    b.chunk_base = reinterpret_cast<int32_t*>(ws + L.chunk_base);
+    b.tiles1 = reinterpret_cast<int32_t*>(ws + L.tiles1);
+    b.tiles2 = reinterpret_cast<int32_t*>(ws + L.tiles2);
+    b.topk_idx = topk_idx;
+    b.topk_w = topk_w;
+    b.topk_wb = reinterpret_cast<uint16_t*>(ws + L.topk_wb);
+    b.perm = perm;
+    b.inv = reinterpret_cast<int32_t*>(ws + L.inv);
+    b.xq = xq;
+    b.sx = sx;
+    // the GEMM tile lists are not asked for: one n-tile per m-tile of the forward's row tiling
+    const int bm = decode_sized((long long)T * top_k, E) ? 32 : 128;
+    return launch_routing(x, router_w, router_b, T, H, E, top_k, bm, 1, 1, false, b,
+                          static_cast<cudaStream_t>(stream), nullptr);
+}
+
+extern "C" moe_status moe_block_weights(const uint8_t* w13_rm, const uint8_t* w2_rm, int H, int I, int E,
+                                        uint8_t* w13, uint8_t* w2, void* stream) {
+    if (H < 1 || I < 1 || E < 1 || H > 16384 || I > 16384 || E > kMaxExperts) return MOE_ERR_INVALID_ARG;
+    if (!w13_rm && !w2_rm) return MOE_ERR_INVALID_ARG;
+    if ((w13_rm && !w13) || (w2_rm && !w2)) return MOE_ERR_INVALID_ARG;
+    if ((w13_rm && (!aligned16(w13_rm) || !aligned16(w13))) || (w2_rm && (!aligned16(w2_rm) || !aligned16(w2))))
+        return MOE_ERR_UNSUPPORTED;
+    const int Hp = pad128(H), Ip = pad128(I);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (w13_rm && launch_block_codes(w13_rm, E, 2 * Ip, Hp, w13, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (w2_rm && launch_block_codes(w2_rm, E, Hp, Ip, w2, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 extern "C" {

@@ -153,6 +153,9 @@ cudaError_t launch_pack_blocks_mx4(const float* src, int E, int rows_src, int co
                                    int gated_I, uint8_t* q, uint8_t* s, cudaStream_t st);
 cudaError_t launch_quantize_rows_mx(const float* in, int rows, int cols, int ld_in, uint8_t* q, uint8_t* s,
                                     cudaStream_t st);
+// Row-major codes [E, rows, cols] (rows, cols multiples of 128) -> blocked
+// [E, rows/128, cols/128, 128, 128]; 16-byte aligned pointers.
+cudaError_t launch_block_codes(const uint8_t* src, int E, int rows, int cols, uint8_t* dst, cudaStream_t st);
 cudaError_t launch_bounded_wait_test(uint64_t timeout_ns, int arrivals, uint32_t* result, cudaStream_t st);
 cudaError_t launch_gemm_gateup(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
                                cudaStream_t st);

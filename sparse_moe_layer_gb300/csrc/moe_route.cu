@@ -901,6 +901,30 @@ cudaError_t launch_pack_blocks(const float* src, int E, int rows_src, int cols, 
     return cudaGetLastError();
 }
 
+// Row-major codes [E, rows, cols] -> blocked [E, rows/128, cols/128, 128, 128]
+// (each 128x128 block 16 KB contiguous, row-major inside): one CTA per block,
+// a thread moves 64 bytes of one row with 16-byte loads and stores.
+__global__ void __launch_bounds__(256) block_codes_kernel(const uint8_t* __restrict__ src, int rows, int cols,
+                                                          uint8_t* __restrict__ dst) {
+    const int bj = blockIdx.x, bi = blockIdx.y, e = blockIdx.z;
+    const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
+    const uint4* in =
+        reinterpret_cast<const uint4*>(src + ((size_t)e * rows + (size_t)bi * 128 + r) * cols + bj * 128 + h * 64);
+    const size_t blk = ((size_t)e * (rows / 128) + bi) * (cols / 128) + bj;
+    uint4* out = reinterpret_cast<uint4*>(dst + blk * 16384 + (size_t)r * 128 + h * 64);
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __ldg(in + i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = v[i];
+}
+
+cudaError_t launch_block_codes(const uint8_t* src, int E, int rows, int cols, uint8_t* dst, cudaStream_t st) {
+    dim3 grid(cols / 128, rows / 128, E);
+    block_codes_kernel<<<grid, 256, 0, st>>>(src, rows, cols, dst);
+    return cudaGetLastError();
+}
+
 // ============================================== stand-alone 1x128 quantiser
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const float* __restrict__ in, int rows, int cols, int ld_in,
                                                             uint8_t* __restrict__ q, float* __restrict__ s) {

@@ -180,10 +180,13 @@ def mx_row_scales(atoms: np.ndarray, count: np.ndarray, offset: np.ndarray, tile
     return out
 
 
-def sample_tokens(idx: np.ndarray, E: int, n: int, seed: int = 0) -> np.ndarray:
+def sample_tokens(idx: np.ndarray, E: int, n: int, seed: int = 0, perm: np.ndarray | None = None,
+                  offset: np.ndarray | None = None, bm: int = 128) -> np.ndarray:
     """Tokens for sampled output checks: first, last, the tokens of the most- and
-    least-loaded (non-empty) experts, and seeded random others."""
-    T = idx.shape[0]
+    least-loaded (non-empty) experts, and seeded random others up to n; with the
+    permutation (perm, offset) also the tokens in the first and last row of every
+    expert's last bm-row GEMM tile (the partial M tile of the grouped GEMMs)."""
+    T, k = idx.shape
     if T <= n:
         return np.arange(T, dtype=np.int32)
     counts = np.bincount(idx.ravel(), minlength=E)
@@ -194,6 +197,12 @@ def sample_tokens(idx: np.ndarray, E: int, n: int, seed: int = 0) -> np.ndarray:
         ts = np.nonzero((idx == e).any(axis=1))[0]
         pick.update(int(t) for t in ts[:2])
         pick.add(int(ts[-1]))
+    if perm is not None and offset is not None:
+        for e in nz:
+            lo, hi = int(offset[e]), int(offset[e + 1])
+            last_tile = lo + (hi - lo - 1) // bm * bm
+            pick.add(int(perm[last_tile]) // k)
+            pick.add(int(perm[hi - 1]) // k)
     rng = np.random.default_rng(seed)
     while len(pick) < n:
         pick.add(int(rng.integers(T)))

@@ -102,12 +102,33 @@ def test_product_sources_do_not_reach_the_oracle():
 
 
 def test_static_scratch_limits_on_the_host(moe):
-    """The entry point without a workspace refuses sizes whose scratch exceeds its
-    32 MiB array, and invalid sizes, before any CUDA call; the decode shapes fit."""
+    """The entry point without a workspace checks its pointers first, then refuses
+    invalid sizes and sizes whose scratch exceeds its 32 MiB array, all before any
+    CUDA call; the decode shapes fit."""
     L = moe.lib()
     nul = [None] * 9
-    assert L.moe_forward_static_scratch(*nul, 8192, 2880, 2880, 128, 4, None, None) == 3  # MOE_ERR_WORKSPACE
-    assert L.moe_forward_static_scratch(*nul, 0, 2880, 2880, 128, 4, None, None) == 1  # MOE_ERR_INVALID_ARG
+    fake = [16 * (i + 1) for i in range(9)]  # non-null, never dereferenced: every check runs on the host first
+    assert L.moe_forward_static_scratch(*nul, 8192, 2880, 2880, 128, 4, None, None) == 1  # null pointers first
+    assert L.moe_forward_static_scratch(*fake, 8192, 2880, 2880, 128, 4, 16, None) == 3  # MOE_ERR_WORKSPACE
+    assert L.moe_forward_static_scratch(*fake, 0, 2880, 2880, 128, 4, 16, None) == 1  # MOE_ERR_INVALID_ARG
     for T, E in ((64, 32), (256, 128)):
         assert 0 < L.moe_workspace_size(T, 2880, 2880, E, 4) <= (32 << 20)
     assert L.moe_workspace_size(8192, 2880, 2880, 128, 4) > (32 << 20)
+
+
+def test_route_debug_and_block_weights_host_checks(moe):
+    L = moe.lib()
+    for f in ("moe_route_debug", "moe_route_workspace_size", "moe_block_weights", "moe_read_static_scratch_status"):
+        assert f in declared_functions()
+    assert L.moe_route_workspace_size(0, 256, 8, 2) == 0
+    assert L.moe_route_workspace_size(64, 256, 8, 9) == 0
+    assert L.moe_route_workspace_size(64, 256, 8, 2) > 0
+    fake = [16 * (i + 1) for i in range(3)]
+    outs = [256 * (i + 1) for i in range(6)]
+    assert L.moe_route_debug(None, None, None, 64, 256, 8, 2, *([None] * 6), None, 0, None) == 1
+    assert L.moe_route_debug(*fake, 0, 256, 8, 2, *outs, 4096, 1 << 20, None) == 1  # T < 1
+    assert L.moe_route_debug(*fake, 64, 256, 8, 2, *outs, 4096 + 8, 1 << 20, None) == 2  # workspace not 256-aligned
+    assert L.moe_route_debug(*fake, 64, 256, 8, 2, *outs, 4096, 16, None) == 3  # short workspace
+    assert L.moe_block_weights(None, None, 256, 256, 8, None, None, None) == 1
+    assert L.moe_block_weights(16, None, 256, 256, 8, None, None, None) == 1  # w13 output missing
+    assert L.moe_block_weights(17, None, 256, 256, 8, 32, None, None) == 2  # misaligned input

@@ -39,9 +39,10 @@ def margin_safe_x(cfg, rw, rb, x=None):
     return x
 
 
-def full_check(moe, layer: Layer, n_sample: int | None = None):
+def full_check(moe, layer: Layer, n_sample: int | None = None, upload: bool = True):
     T, k, E = layer.T, layer.k, layer.E
-    layer.to_device()
+    if upload:
+        layer.to_device()
     out, v, ws = layer.run_gpu()
     assert moe.read_device_status(ws) == 0
     r = layer.oracle_router()
@@ -73,7 +74,8 @@ def full_check(moe, layer: Layer, n_sample: int | None = None):
     assert np.array_equal(v["xq"].cpu().numpy(), xq[tok_of_row])
     assert np.array_equal(v["sx"].cpu().numpy(), sx[tok_of_row])
     # layer output (all tokens, or a sample including the most/least loaded experts)
-    tokens = np.arange(T, dtype=np.int32) if n_sample is None else sample_tokens(r["idx"], E, n_sample)
+    tokens = (np.arange(T, dtype=np.int32) if n_sample is None else
+              sample_tokens(r["idx"], E, n_sample, perm=p["perm"], offset=p["offset"], bm=bm))
     o_out, inter = layer.oracle_forward(tokens, r["idx"])
     rel = check_output(torch_bf16_to_np(out)[tokens], o_out)
     # requantised h of the same (token, slot) rows
@@ -227,8 +229,38 @@ def test_repeated_calls_are_bit_identical(moe):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-@pytest.mark.parametrize("name,n_sample", [("oss20b_decode", None), ("oss120b_decode", 32),
-                                           ("oss120b_prefill", 24), ("qwen235b_prefill", 24)])
+@pytest.mark.parametrize("name,n_sample", [("oss20b_decode", None), ("oss120b_decode", 64),
+                                           ("oss120b_prefill", 128), ("qwen235b_prefill", 128)])
 def test_layer_shapes_full_size(moe, name, n_sample):
     full_check(moe, Layer(synth.config(name)), n_sample=n_sample)
     torch.cuda.empty_cache()
+
+
+def _tiny_token_layer(name, T, E, k, tiny_t):
+    """A layer whose token tiny_t has x scaled by 2^-40 and zero gate/up biases, so
+    that its h = silu(g) * u has a group amax far below 2^-64 (the quantiser's IEEE
+    division range); the router bias alone routes it (distinct biases, margin 0.1)."""
+    cfg = synth.LayerConfig(name, T, 256, 256, E, k, 13, "normal", "zero")
+    rw, _ = synth.router(cfg)
+    rb = bf16_bits(np.float32(0.1) * np.arange(E, 0, -1, dtype=np.float32))
+    x = synth.x_rows(cfg)
+    xt = synth.bf16_to_f32(x[tiny_t]) * np.float32(2.0 ** -40)  # exact: a power of two
+    x[tiny_t] = bf16_bits(xt)
+    x = margin_safe_x(cfg, rw, rb, x)
+    b13, b2 = synth.expert_biases(cfg)
+    layer = Layer(cfg, x=x, rw=rw, rb=rb, b13=np.zeros_like(b13), b2=b2)
+    assert np.array_equal(layer.x[tiny_t], x[tiny_t])  # the tiny row kept its draw
+    return layer
+
+
+@pytest.mark.parametrize("T,E,k", [(16, 4, 2), (600, 4, 2)], ids=["decode_tile", "prefill_tile"])
+def test_requant_of_a_token_with_tiny_h(moe, T, E, k):
+    # decode tiles: the token's lane makes its whole warp take IEEE division;
+    # prefill tiles: the token's row thread takes it alone
+    tiny_t = 5
+    layer = _tiny_token_layer(f"tiny_h_{T}", T, E, k, tiny_t)
+    out, _, _ = full_check(moe, layer)
+    _, v, _ = layer.run_gpu()
+    rows = v["inv"].cpu().numpy()[tiny_t * k:(tiny_t + 1) * k]
+    sh = v["sh"].cpu().numpy()[rows]
+    assert np.all(sh < np.float32(2.0 ** -64 / 448)) and np.all(sh > 0), sh  # amax < 2^-64: the slow path ran
