@@ -71,7 +71,8 @@ typedef enum {
  * After moe_forward completes they hold that call's values; tests read them. */
 typedef struct {
     size_t total_bytes;
-    size_t status;     /* uint32[64]: [0] device error word, [1] tile total GEMM1, [2] tile total GEMM2 */
+    size_t status;     /* uint32[64]: [0] device error word, [1] tile total GEMM1, [2] tile total GEMM2,
+                          [3] rows per M tile */
     size_t hist;       /* int32 [ceil(T/256), E] tokens per (256-token chunk, expert), then 1 arrival counter */
     size_t count;      /* int32 [E]     rows per expert */
     size_t offset;     /* int32 [E+1]   first row of each expert (exclusive scan of count) */

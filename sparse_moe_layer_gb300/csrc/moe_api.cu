@@ -33,6 +33,7 @@ bool sizes_ok(int T, int H, int I, int E, int k) {
 // kernels with 32-row token tiles; larger ones the 128-row tile kernels.
 inline bool decode_sized(long long R, int E) { return R <= 64LL * E; }
 
+
 void layout_of(int T, int H, int I, int E, int k, moe_workspace_layout* L, bool mx = false) {
     const size_t R = (size_t)T * k;
     const size_t Hp = pad128(H), Ip = pad128(I);
@@ -146,8 +147,9 @@ enum WeightFormat { kBlock128 = 0, kMxfp8 = 1, kMxfp4 = 2 };
 
 // What the router and the permutation kernel write (device pointers).
 struct RoutingBuffers {
-    uint32_t* status;     // uint32[64], zeroed here
-    int32_t* hist;        // [ceil(T/256), E] + 1 arrival counter, zeroed here (directly after status)
+    uint32_t* status;     // uint32[64]; it and the zero_bytes after it are zeroed here
+    size_t zero_bytes;    // the status words, the histogram and any counters placed after them
+    int32_t* hist;        // [ceil(T/256), E] + 1 arrival counter (inside the zeroed bytes)
     int32_t* count;       // [E]
     int32_t* offset;      // [E+1]
     int32_t* chunk_base;  // [ceil(T/256), E]
@@ -171,10 +173,9 @@ static moe_status launch_routing(const void* x, const void* router_w, const void
                                  cudaStream_t st, cudaEvent_t mid) {
     const int Hp = pad128(H);
     const int nch = (T + kChunkTokens - 1) / kChunkTokens;
-    // status words and the (chunk, expert) histogram with its arrival counter start at zero
-    const size_t zero_bytes = reinterpret_cast<uint8_t*>(b.hist + (size_t)nch * E + 1) -
-                              reinterpret_cast<uint8_t*>(b.status);
-    if (cudaMemsetAsync(b.status, 0, zero_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+    // status words, the (chunk, expert) histogram with its arrival counter, and
+    // the counters after it start at zero
+    if (cudaMemsetAsync(b.status, 0, b.zero_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
     RouteParams rp;
     rp.x = static_cast<const uint16_t*>(x);
     rp.rw = static_cast<const uint16_t*>(router_w);
@@ -192,7 +193,6 @@ static moe_status launch_routing(const void* x, const void* router_w, const void
     rp.topk_wb = b.topk_wb;
     rp.hist = b.hist;
     rp.done = b.hist + (size_t)nch * E;
-    rp.scan_in_router = router_scans(T) ? 1 : 0;
     rp.count = b.count;
     rp.offset = b.offset;
     rp.chunk_base = b.chunk_base;
@@ -221,17 +221,10 @@ static moe_status launch_routing(const void* x, const void* router_w, const void
     pp.tokens_per_cta = (T > 2048 && 8LL * ((H + 7) & ~7) * 2 <= 96 * 1024) ? 8 : 1;
     pp.topk_idx = b.topk_idx;
     pp.chunk_base = b.chunk_base;
-    pp.scan_here = router_scans(T) ? 0 : 1;
-    pp.nchunks = nch;
     pp.bm = bm;
     pp.nt1 = nt1;
-    pp.nt2 = nt2;
-    pp.hist = b.hist;
-    pp.count = b.count;
     pp.offset = b.offset;
     pp.tiles1 = b.tiles1;
-    pp.tiles2 = b.tiles2;
-    pp.status = b.status;
     pp.perm = b.perm;
     pp.inv = b.inv;
     pp.xq = b.xq;
@@ -376,6 +369,7 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     const int nt2 = decode ? Hp / 128 : (Hp / 128 + 1) / 2;
     RoutingBuffers rb;
     rb.status = reinterpret_cast<uint32_t*>(ws + L.status);
+    rb.zero_bytes = L.count - L.status;
     rb.hist = reinterpret_cast<int32_t*>(ws + L.hist);
     rb.count = reinterpret_cast<int32_t*>(ws + L.count);
     rb.offset = reinterpret_cast<int32_t*>(ws + L.offset);
@@ -661,6 +655,7 @@ extern "C" moe_status moe_route_debug(const void* x, const void* router_w, const
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     RoutingBuffers b;
     b.status = reinterpret_cast<uint32_t*>(ws + L.status);
+    b.zero_bytes = L.count - L.status;
     b.hist = reinterpret_cast<int32_t*>(ws + L.hist);
     b.count = reinterpret_cast<int32_t*>(ws + L.count);
     b.offset = offset;

@@ -15,7 +15,13 @@ constexpr int kChunkTokens = 256;  // token chunk of the expert histogram
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // every device wait gives up after 2 s
 
 // status words (uint32 array at the head of the workspace)
-enum : int { kStatusError = 0, kStatusTiles1 = 1, kStatusTiles2 = 2, kStatusTileRows = 3, kStatusWords = 64 };
+enum : int {
+    kStatusError = 0,
+    kStatusTiles1 = 1,
+    kStatusTiles2 = 2,
+    kStatusTileRows = 3,
+    kStatusWords = 64
+};
 enum : uint32_t { kErrTimeoutProducer = 1u, kErrTimeoutMma = 2u, kErrTimeoutEpilogue = 4u };
 
 // ------------------------------------------------------------ conversion ----

@@ -156,13 +156,13 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), 512);
-    // everything above overlaps the previous kernel's tail; from here on this
-    // kernel reads what the previous kernels wrote
-    pdl_wait();
+    // Everything up to pdl_wait overlaps the previous kernel's tail.  The tile
+    // lists come from the router's scan, which had completed before the kernel
+    // ahead of this one let it be scheduled; read them from L2 now.
     for (int i = tid; i <= E; i += C::THREADS) {
-        s_tiles[i] = p.tiles[i];
-        s_off[i] = p.offset[i];
-        if (i < E) s_cnt[i] = p.count[i];
+        s_tiles[i] = __ldcg(p.tiles + i);
+        s_off[i] = __ldcg(p.offset + i);
+        if (i < E) s_cnt[i] = __ldcg(p.count + i);
     }
     tc_fence_before();
     __syncthreads();
@@ -171,6 +171,26 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
     const int total = s_tiles[E];
     volatile int* abort_p = &abort_flag;
     uint32_t* err = p.status + kStatusError;
+    // The weights are inputs of the layer: the producer fills the first
+    // stages' weight boxes before waiting for the previous kernel, whose
+    // output (the activation rows) it loads after the wait.
+    int pre = 0;  // stages whose weight boxes are in flight before the wait
+    if (warp == 0 && lane == 0) {
+        for (int tile = blockIdx.x; tile < total && pre < C::STAGES; tile += gridDim.x) {
+            const TileInfo ti = decode_tile(tile, s_tiles, s_off, s_cnt, E);
+            const int blk0 = (ti.e * p.sw_rowblocks + weight_block<GATED>(p, ti.nt, 0)) * p.KB;
+            const int blk1 = (ti.e * p.sw_rowblocks + weight_block<GATED>(p, ti.nt, 1)) * p.KB;
+            for (int kb = 0; kb < p.KB && pre < C::STAGES; ++kb, ++pre) {
+                const uint32_t fb = smem_u32(&full_bar[pre]);
+                mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                const uint32_t b_dst = smem_u32(smem + pre * C::STAGE_BYTES) + C::A_BYTES;
+                tma_load_2d(b_dst, &tmB, 0, (blk0 + kb) * 128, fb);
+                tma_load_2d(b_dst + 128 * 128, &tmB, 0, (blk1 + kb) * 128, fb);
+            }
+        }
+    }
+    // from here on this kernel reads what the previous kernels wrote
+    pdl_wait();
     // Every CTA of this persistent grid is resident, so the next kernel may be
     // scheduled now: its CTAs land on SMs as this grid's CTAs exit and run
     // their prologue there while the last tiles finish.
@@ -192,17 +212,21 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
                 const int blk0 = (ti.e * p.sw_rowblocks + weight_block<GATED>(p, ti.nt, 0)) * p.KB;
                 const int blk1 = (ti.e * p.sw_rowblocks + weight_block<GATED>(p, ti.nt, 1)) * p.KB;
                 for (int kb = 0; kb < p.KB; ++kb) {
-                    if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) {
-                        ok = false;
-                        break;
-                    }
                     const uint32_t fb = smem_u32(&full_bar[stage]);
-                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
                     const uint32_t a_dst = smem_u32(smem + stage * C::STAGE_BYTES);
                     const uint32_t b_dst = a_dst + C::A_BYTES;
+                    if (pre > 0) {
+                        --pre;  // first use of this stage: its weights went out before the wait
+                    } else {
+                        if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                        tma_load_2d(b_dst, &tmB, 0, (blk0 + kb) * 128, fb);
+                        tma_load_2d(b_dst + 128 * 128, &tmB, 0, (blk1 + kb) * 128, fb);
+                    }
                     tma_load_2d(a_dst, &tmA, kb * 128, ti.row0, fb);
-                    tma_load_2d(b_dst, &tmB, 0, (blk0 + kb) * 128, fb);
-                    tma_load_2d(b_dst + 128 * 128, &tmB, 0, (blk1 + kb) * 128, fb);
                     filled |= 1u << stage;
                     if (++stage == C::STAGES) {
                         stage = 0;

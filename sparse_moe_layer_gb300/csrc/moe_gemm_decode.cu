@@ -141,11 +141,12 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
         tma_prefetch_desc(&tmX);
     }
     if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), C::TMEM_COLS);
-    pdl_wait();
+    // The tile lists come from the router's scan, which had completed before
+    // the kernel ahead of this one let it be scheduled; read them from L2 now.
     for (int i = tid; i <= E; i += C::THREADS) {
-        s_tiles[i] = p.tiles[i];
-        s_off[i] = p.offset[i];
-        if (i < E) s_cnt[i] = p.count[i];
+        s_tiles[i] = __ldcg(p.tiles + i);
+        s_off[i] = __ldcg(p.offset + i);
+        if (i < E) s_cnt[i] = __ldcg(p.count + i);
     }
     tc_fence_before();
     __syncthreads();
@@ -154,6 +155,26 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
     const int total = s_tiles[E];
     volatile int* abort_p = &abort_flag;
     uint32_t* err = p.status + kStatusError;
+    // The weights are inputs of the layer: the producer fills the first
+    // stages' weight boxes before waiting for the previous kernel, whose
+    // output (the token rows) it loads after the wait.
+    int pre = 0;  // stages whose weight boxes are in flight before the wait
+    if (warp == 0 && lane == 0) {
+        for (int tile = blockIdx.x; tile < total && pre < nst; tile += gridDim.x) {
+            const DecTile ti = decode_dec_tile(tile, s_tiles, s_off, s_cnt, E);
+            const int wblk = (ti.e * p.sw_rowblocks + ti.nt) * p.KB;
+            const int ublk = GATED ? (p.up_rows / 128) * p.KB : 0;
+            const int nxb = (ti.rows + kDecXBoxRows - 1) / kDecXBoxRows;
+            for (int kb = 0; kb < p.KB && pre < nst; ++kb, ++pre) {
+                const uint32_t fb = smem_u32(&full_bar[pre]);
+                mbar_arrive_expect_tx(fb, C::W_BYTES + nxb * kDecXBoxRows * 128);
+                const uint32_t w_dst = smem_u32(smem + pre * C::STAGE_BYTES);
+                tma_load_2d(w_dst, &tmW, 0, (wblk + kb) * 128, fb);
+                if (GATED) tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb) * 128, fb);
+            }
+        }
+    }
+    pdl_wait();
     pdl_allow_dependents();
 
     if (warp == 0) {
@@ -169,15 +190,19 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                 const int ublk = GATED ? (p.up_rows / 128) * p.KB : 0;
                 const int nxb = (ti.rows + kDecXBoxRows - 1) / kDecXBoxRows;
                 for (int kb = 0; kb < p.KB; ++kb) {
-                    if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) {
-                        ok = false;
-                        break;
-                    }
                     const uint32_t fb = smem_u32(&full_bar[stage]);
-                    mbar_arrive_expect_tx(fb, C::W_BYTES + nxb * kDecXBoxRows * 128);
                     const uint32_t w_dst = smem_u32(smem + stage * C::STAGE_BYTES);
-                    tma_load_2d(w_dst, &tmW, 0, (wblk + kb) * 128, fb);
-                    if (GATED) tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb) * 128, fb);
+                    if (pre > 0) {
+                        --pre;  // first use of this stage: its weights went out before the wait
+                    } else {
+                        if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(fb, C::W_BYTES + nxb * kDecXBoxRows * 128);
+                        tma_load_2d(w_dst, &tmW, 0, (wblk + kb) * 128, fb);
+                        if (GATED) tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb) * 128, fb);
+                    }
                     // only the boxes that hold rows of this tile; the MMA reads stale shared
                     // memory for the other token columns, whose results are never stored
                     for (int b = 0; b < nxb; ++b)
@@ -263,7 +288,15 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                 m[c] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + (c >> 7) * p.N_real + n)) : 0.f;
             }
             const int rtok = min(ti.row0 + lane, p.R - 1);
-            for (int kb = 0; kb < p.KB; ++kb) m[M.sa + kb * 32 + lane] = __ldg(p.sa + (size_t)kb * p.R + rtok);
+            // the tile's token scales, eight K blocks in flight per lane
+            for (int kb = 0; kb < p.KB; kb += 8) {
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = kb + i < p.KB ? __ldg(p.sa + (size_t)(kb + i) * p.R + rtok) : 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (kb + i < p.KB) m[M.sa + (kb + i) * 32 + lane] = v[i];
+            }
             const float* sw_g = p.sw + ((size_t)ti.e * p.sw_rowblocks + ti.nt) * p.KB;
             for (int kb = lane; kb < p.KB; kb += 32) {
                 m[M.sw + kb] = __ldg(sw_g + kb);

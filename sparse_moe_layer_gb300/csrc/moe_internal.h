@@ -21,8 +21,10 @@ struct RouteParams {
     float* topk_w;
     uint16_t* topk_wb;
     int32_t* hist;    // [nchunks, E], zeroed before the launch
-    int32_t* done;    // arrival counter of finished router CTAs, zeroed before the launch
-    int scan_in_router;  // 1: the last router CTA scans the histogram (else the permutation kernel does)
+    int32_t* done;    // arrival counter of finished router CTAs, zeroed before the launch: the last
+                      // one scans the histogram into count, offset, chunk_base and the tile lists,
+                      // which are final when the router grid completes (the GEMMs read them before
+                      // they wait for the permutation kernel)
     int32_t* count;
     int32_t* offset;
     int32_t* chunk_base;
@@ -35,16 +37,12 @@ struct PermuteParams {
     const uint16_t* x;
     int T, H, Hp, E, k;
     int tokens_per_cta;
+    int early_dependents;  // set at launch: 1 when the grid is one wave (the next kernel may start early)
     const int32_t* topk_idx;
     const int32_t* chunk_base;
-    // decode-sized batches: the router did not scan the histogram, this kernel does
-    int scan_here, nchunks, bm, nt1, nt2;
-    const int32_t* hist;
-    int32_t* count;
-    int32_t* offset;
-    int32_t* tiles1;
-    int32_t* tiles2;
-    uint32_t* status;
+    int bm, nt1;
+    const int32_t* offset;  // MXFP8: first row and first m-tile of each expert (scale atom positions)
+    const int32_t* tiles1;
     int32_t* perm;
     int32_t* inv;
     int R;        // T * k
@@ -131,7 +129,6 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-bool router_scans(int T);  // large batches: the router scans, small ones: the permutation kernel
 cudaError_t launch_router(const RouteParams& p, cudaStream_t st);
 // Tensor-core router: the padded expert count NP it would use (32, 64, 128 or
 // 256), or 0 when the layer takes the cluster kernel above (fewer than 2048

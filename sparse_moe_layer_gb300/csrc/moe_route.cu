@@ -107,26 +107,52 @@ __device__ void finish_scan(const RouteParams& p, int* buf, int cap) {
         s_count[e] = run;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int off = 0, t1 = 0, t2 = 0;
-        for (int e = 0; e < p.E; ++e) {
-            const int c = s_count[e];
-            s_off[e] = off;
-            p.offset[e] = off;
-            p.count[e] = c;
-            const int mt = (c + p.bm - 1) / p.bm;
-            p.tiles1[e] = t1;
-            p.tiles2[e] = t2;
-            off += c;
-            t1 += mt * p.nt1;
-            t2 += mt * p.nt2;
+    if (threadIdx.x < 32) {
+        // exclusive scans of the counts and of the m-tiles over the experts by
+        // one warp: lane l owns experts [8l, 8l+8) (E <= 256)
+        const int lane = threadIdx.x;
+        int cnt[8], mt[8];
+        int tc = 0, tm = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            cnt[i] = e < p.E ? s_count[e] : 0;
+            mt[i] = (cnt[i] + p.bm - 1) / p.bm;
+            tc += cnt[i];
+            tm += mt[i];
         }
-        p.offset[p.E] = off;
-        p.tiles1[p.E] = t1;
-        p.tiles2[p.E] = t2;
-        p.status[kStatusTiles1] = (uint32_t)t1;
-        p.status[kStatusTiles2] = (uint32_t)t2;
-        p.status[kStatusTileRows] = (uint32_t)p.bm;
+        int ic = tc, im = tm;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int vc = __shfl_up_sync(0xffffffffu, ic, o);
+            const int vm = __shfl_up_sync(0xffffffffu, im, o);
+            if (lane >= o) {
+                ic += vc;
+                im += vm;
+            }
+        }
+        int off = ic - tc, mts = im - tm;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            if (e < p.E) {
+                s_off[e] = off;
+                p.offset[e] = off;
+                p.count[e] = cnt[i];
+                p.tiles1[e] = mts * p.nt1;
+                p.tiles2[e] = mts * p.nt2;
+            }
+            off += cnt[i];
+            mts += mt[i];
+        }
+        if (lane == 31) {
+            p.offset[p.E] = off;
+            p.tiles1[p.E] = mts * p.nt1;
+            p.tiles2[p.E] = mts * p.nt2;
+            p.status[kStatusTiles1] = (uint32_t)(mts * p.nt1);
+            p.status[kStatusTiles2] = (uint32_t)(mts * p.nt2);
+            p.status[kStatusTileRows] = (uint32_t)p.bm;
+        }
     }
     __syncthreads();
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
@@ -313,7 +339,7 @@ __global__ void __launch_bounds__(256) router_kernel(RouteParams p, int cpc) {
     }
     // no CTA leaves while another may still read its partial tile
     cluster_sync_all();
-    if (p.scan_in_router && last_to_arrive(p.done, gridDim.x))
+    if (last_to_arrive(p.done, gridDim.x))
         finish_scan(p, reinterpret_cast<int*>(smem), (int)(C::SMEM / 4));
 }
 
@@ -348,7 +374,6 @@ static cudaError_t launch_router_t(const RouteParams& p, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, router_kernel<NTW, VEC, TOK>, p, cpc);
 }
 
-bool router_scans(int T) { return T >= 512; }
 
 template <int NTW, int TOK>
 static cudaError_t launch_router_v(const RouteParams& p, cudaStream_t st) {
@@ -553,7 +578,7 @@ __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    if (p.scan_in_router && last_to_arrive(p.done, gridDim.x))
+    if (last_to_arrive(p.done, gridDim.x))
         finish_scan(p, reinterpret_cast<int*>(smem), C::STAGES * C::STAGE_BYTES / 4);
 }
 
@@ -619,80 +644,19 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
         }
     }
     pdl_wait();
+    // The router has completed (its scan wrote the tile lists), so the gate/up
+    // GEMM may be scheduled now: it reads those lists and streams its first
+    // weight stages while this kernel quantises x, then waits for it.  Only
+    // for a grid of one wave: the GEMM's CTAs would otherwise hold SMs that
+    // this kernel's later CTAs need.
+    if (p.early_dependents) pdl_allow_dependents();
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) s_pre[e] = 0;
-    if (p.scan_here) {
-        // offsets from the (chunk, expert) histogram: count[e], its exclusive
-        // scan, and the first row of this chunk for every expert
-        for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
-            int before = 0, total = 0;
-            for (int c = 0; c < p.nchunks; ++c) {
-                const int h = __ldcg(&p.hist[(size_t)c * p.E + e]);
-                if (c < chunk) before += h;
-                total += h;
-            }
-            s_base[e] = before;
-            s_pre[e] = total;  // reused below as the prefix counter; counts kept in s_base/offset
-        }
-        __syncthreads();
-        if (threadIdx.x < 32) {
-            // exclusive scans over the experts by one warp: lane l owns experts [8l, 8l+8)
-            const int lane = threadIdx.x;
-            int cnt[8], mt[8];
-            int tc = 0, tm = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = lane * 8 + i;
-                cnt[i] = e < p.E ? s_pre[e] : 0;
-                mt[i] = (cnt[i] + p.bm - 1) / p.bm;
-                tc += cnt[i];
-                tm += mt[i];
-            }
-            int ic = tc, im = tm;  // inclusive scans of the lane totals
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int vc = __shfl_up_sync(0xffffffffu, ic, o);
-                const int vm = __shfl_up_sync(0xffffffffu, im, o);
-                if (lane >= o) {
-                    ic += vc;
-                    im += vm;
-                }
-            }
-            int off = ic - tc, mts = im - tm;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = lane * 8 + i;
-                if (e < p.E) {
-                    s_base[e] += off;
-                    s_eoff[e] = off;
-                    s_emt[e] = mts;
-                    if (blockIdx.x == 0) {
-                        p.offset[e] = off;
-                        p.count[e] = cnt[i];
-                        p.tiles1[e] = mts * p.nt1;
-                        p.tiles2[e] = mts * p.nt2;
-                    }
-                }
-                off += cnt[i];
-                mts += mt[i];
-            }
-            if (blockIdx.x == 0 && lane == 31) {
-                p.offset[p.E] = off;
-                p.tiles1[p.E] = mts * p.nt1;
-                p.tiles2[p.E] = mts * p.nt2;
-                p.status[kStatusTiles1] = (uint32_t)(mts * p.nt1);
-                p.status[kStatusTiles2] = (uint32_t)(mts * p.nt2);
-                p.status[kStatusTileRows] = (uint32_t)p.bm;
-            }
-        }
-        __syncthreads();
-        for (int e = threadIdx.x; e < p.E; e += blockDim.x) s_pre[e] = 0;
-    } else {
-        for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
-            s_base[e] = p.chunk_base[(size_t)chunk * p.E + e];
-            if (p.mx) {
-                s_eoff[e] = p.offset[e];
-                s_emt[e] = p.tiles1[e] / p.nt1;
-            }
+    // the router scanned the histogram: this chunk's first row of every expert
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+        s_base[e] = p.chunk_base[(size_t)chunk * p.E + e];
+        if (p.mx) {
+            s_eoff[e] = p.offset[e];
+            s_emt[e] = p.tiles1[e] / p.nt1;
         }
     }
     __syncthreads();
@@ -786,8 +750,12 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteParams p) {
     }
 }
 
-cudaError_t launch_permute_quant(const PermuteParams& p, cudaStream_t st) {
+cudaError_t launch_permute_quant(const PermuteParams& p_in, cudaStream_t st) {
+    PermuteParams p = p_in;
     int grid = (p.T + p.tokens_per_cta - 1) / p.tokens_per_cta;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    p.early_dependents = grid <= sms ? 1 : 0;
     const size_t sm = (size_t)p.tokens_per_cta * ((p.H + 7) & ~7) * 2;
     cudaError_t e = cudaFuncSetAttribute(permute_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;

@@ -90,3 +90,19 @@ def test_flush_writes_one_buffer_and_reads_the_other():
     bench.flush_l2(w, r, 0x1A5)
     assert int(w.min()) == int(w.max()) == 0xA5  # the step index's low byte, every byte written
     assert int(r.abs().sum()) == 0  # the read buffer is only read
+
+
+def test_baseline_sample_includes_the_extreme_experts():
+    rng = np.random.default_rng(3)
+    idx = rng.integers(0, 8, (200, 2))
+    idx[:, 1] = np.where(idx[:, 1] == idx[:, 0], (idx[:, 0] + 1) % 8, idx[:, 1])  # two distinct experts per token
+    counts = np.bincount(idx.ravel(), minlength=8)
+    nz = np.nonzero(counts)[0]
+    most, least = nz[np.argmax(counts[nz])], nz[np.argmin(counts[nz])]
+    tokens, desc = bench.sample_for_baseline(idx, 8, 40)
+    assert len(tokens) == 40 and np.all(np.diff(tokens) > 0)
+    for e in (most, least):
+        assert (idx[tokens] == e).any(), e
+    assert f"expert {least}" in desc and f"expert {most}" in desc
+    all_tokens, _ = bench.sample_for_baseline(idx, 8, 10 ** 6)  # a budget above the batch takes all of it
+    assert np.array_equal(all_tokens, np.arange(200))
