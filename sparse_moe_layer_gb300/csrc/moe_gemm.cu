@@ -191,10 +191,10 @@ __global__ void __launch_bounds__(GemmCfg<GATED>::THREADS, 1)
     }
     // from here on this kernel reads what the previous kernels wrote
     pdl_wait();
-    // Every CTA of this persistent grid is resident, so the next kernel may be
-    // scheduled now: its CTAs land on SMs as this grid's CTAs exit and run
-    // their prologue there while the last tiles finish.
-    pdl_allow_dependents();
+    // No early launch_dependents: the next kernel starts when this grid
+    // completes.  Releasing it here made the replayed qwen235b_prefill step
+    // 93 us slower (oss120b_prefill 24 us), although its CTAs could only take
+    // SMs as this grid's CTAs exit.
 
     if (warp < 4) {
         regs_release<C::WG0_REGS>();

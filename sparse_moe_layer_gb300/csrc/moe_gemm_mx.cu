@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(MxCfg<GATED, FP4W>::THREADS, 1)
     const int total = s_tiles[E];
     volatile int* abort_p = &abort_flag;
     uint32_t* err = p.status + kStatusError;
-    pdl_allow_dependents();
+    // no early launch_dependents at prefill sizes (see the 128x128 prefill GEMM)
 
     if (warp == 0) {
         if (lane == 0) {
