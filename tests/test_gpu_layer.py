@@ -264,3 +264,14 @@ def test_requant_of_a_token_with_tiny_h(moe, T, E, k):
     rows = v["inv"].cpu().numpy()[tiny_t * k:(tiny_t + 1) * k]
     sh = v["sh"].cpu().numpy()[rows]
     assert np.all(sh < np.float32(2.0 ** -64 / 448)) and np.all(sh > 0), sh  # amax < 2^-64: the slow path ran
+
+
+@pytest.mark.parametrize("name,T,H,I,E,k", [
+    ("max_experts_topk", 48, 256, 256, 256, 8),       # E and top_k at their limits (router pads 256 experts)
+    ("max_hidden_decode", 8, 16384, 128, 4, 2),        # H at its limit: 128 K blocks in the gate/up GEMM
+    ("max_hidden_prefill", 600, 16384, 128, 4, 2),     # the same through the 128-row tile GEMMs
+    ("max_inter_prefill", 600, 128, 16384, 4, 2),      # I at its limit: 128 h blocks, 128 K blocks in the down GEMM
+], ids=lambda v: v if isinstance(v, str) else None)
+def test_size_limits(moe, name, T, H, I, E, k):
+    full_check(moe, _adhoc(name, T, H, I, E, k), n_sample=None if T <= 64 else 48)
+    torch.cuda.empty_cache()

@@ -47,9 +47,10 @@ def adhoc(name, T, H, I, E, k, seed=11, rb=None):
     return Layer(cfg, x=margin_safe_x(cfg, rw, rb), rw=rw, rb=rb, mx=True)
 
 
-def full_check_mx(moe, layer: Layer, n_sample: int | None = None):
+def full_check_mx(moe, layer: Layer, n_sample: int | None = None, upload: bool = True):
     T, k, E, Hp, Ip = layer.T, layer.k, layer.E, layer.Hp, layer.Ip
-    layer.to_device()
+    if upload:
+        layer.to_device()
     out, v, ws = layer.run_gpu()
     assert moe.read_device_status(ws) == 0
     r = layer.oracle_router()
