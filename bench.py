@@ -90,23 +90,30 @@ def algorithmic(cfg, counts: np.ndarray, mx: bool = False, fp4: bool = False) ->
                 gemm1_flops=2 * R * 2 * I * H, gemm2_flops=2 * R * H * I, router_flops=2 * T * E * H)
 
 
-def source_digest(mx: bool = False) -> str:
-    """Digest of the GEMM kernels' sources (ncu traffic is valid only for the source it was taken on)."""
+def source_digest(mx: bool = False, decode: bool | None = None) -> str:
+    """Digest of a GEMM kernel's sources (ncu traffic is valid only for the source it
+    was taken on): the file of the kernel (MX kernels; the 128x128 prefill or
+    decode kernels; both 128x128 files when `decode` is None) and the shared headers."""
     h = hashlib.sha256()
-    files = ("moe_gemm_mx.cu",) if mx else ("moe_gemm.cu", "moe_gemm_decode.cu")
+    if mx:
+        files = ("moe_gemm_mx.cu",)
+    elif decode is None:
+        files = ("moe_gemm.cu", "moe_gemm_decode.cu")
+    else:
+        files = ("moe_gemm_decode.cu",) if decode else ("moe_gemm.cu",)
     for f in files + ("moe_device.cuh", "moe_internal.h"):
         with open(os.path.join(ROOT, "sparse_moe_layer_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, cfg_name: str, mx: bool = False):
+def recorded_traffic(kernel: str, cfg_name: str, mx: bool = False, decode: bool | None = None):
     """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel source."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             t = json.load(f)
         rec = t.get(f"{kernel}@{cfg_name}")
-        if rec and rec.get("source_digest") == source_digest(mx):
+        if rec and rec.get("source_digest") == source_digest(mx, None if mx else decode):
             return int(rec["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -536,7 +543,7 @@ def main():
         roof = dict(bound="hbm", achieved=alg["gemm1_bytes"] / g1_s / 1e9, peak=pk["hbm"], unit="GB/s")
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = recorded_traffic("gemm_gateup_mx4" if fp4 else "gemm_gateup_mx" if mx else "gemm_gateup",
-                                       cfg.name, mx)
+                                       cfg.name, mx, decode=not prefill)
     if fp4:
         roof["kernel"] = ("moe_gemm_mx_kernel<true, FP4W> (block-scaled e4m3 x e2m1 gate/up GEMM + SwiGLU + MX "
                           "requant)" if prefill else

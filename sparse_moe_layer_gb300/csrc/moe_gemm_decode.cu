@@ -40,7 +40,11 @@ struct DecCfg {
     static constexpr int BT = 32;                         // token rows per tile (MMA N)
     static constexpr int W_BYTES = (GATED ? 2 : 1) * 128 * 128;
     static constexpr int X_BYTES = BT * 128;
-    static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
+    // K blocks per ring stage (one: two per stage were measured slower for both
+    // GEMMs, which stream at their bound with one)
+    static constexpr int KPS = GATED ? MOE_DEC_KPS_GATEUP : MOE_DEC_KPS_DOWN;
+    // stage: the KPS weight blocks, then the KPS token-row blocks
+    static constexpr int STAGE_BYTES = KPS * (W_BYTES + X_BYTES);
     static constexpr int MAX_STAGES = 16;                 // the ring takes what shared memory is left (launch)
     static constexpr int ACC_COLS = GATED ? 2 * BT : BT;  // TMEM columns of one accumulation buffer
     static constexpr int TMEM_COLS = 512;
@@ -165,12 +169,15 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
             const int wblk = (ti.e * p.sw_rowblocks + ti.nt) * p.KB;
             const int ublk = GATED ? (p.up_rows / 128) * p.KB : 0;
             const int nxb = (ti.rows + kDecXBoxRows - 1) / kDecXBoxRows;
-            for (int kb = 0; kb < p.KB && pre < nst; ++kb, ++pre) {
+            for (int kb = 0; kb < p.KB && pre < nst; kb += C::KPS, ++pre) {
+                const int nk = min(C::KPS, p.KB - kb);
                 const uint32_t fb = smem_u32(&full_bar[pre]);
-                mbar_arrive_expect_tx(fb, C::W_BYTES + nxb * kDecXBoxRows * 128);
-                const uint32_t w_dst = smem_u32(smem + pre * C::STAGE_BYTES);
-                tma_load_2d(w_dst, &tmW, 0, (wblk + kb) * 128, fb);
-                if (GATED) tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb) * 128, fb);
+                mbar_arrive_expect_tx(fb, nk * (C::W_BYTES + nxb * kDecXBoxRows * 128));
+                for (int i = 0; i < nk; ++i) {
+                    const uint32_t w_dst = smem_u32(smem + pre * C::STAGE_BYTES + i * C::W_BYTES);
+                    tma_load_2d(w_dst, &tmW, 0, (wblk + kb + i) * 128, fb);
+                    if (GATED) tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb + i) * 128, fb);
+                }
             }
         }
     }
@@ -189,9 +196,10 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                 const int wblk = (ti.e * p.sw_rowblocks + ti.nt) * p.KB;
                 const int ublk = GATED ? (p.up_rows / 128) * p.KB : 0;
                 const int nxb = (ti.rows + kDecXBoxRows - 1) / kDecXBoxRows;
-                for (int kb = 0; kb < p.KB; ++kb) {
+                for (int kb = 0; kb < p.KB; kb += C::KPS) {
+                    const int nk = min(C::KPS, p.KB - kb);
                     const uint32_t fb = smem_u32(&full_bar[stage]);
-                    const uint32_t w_dst = smem_u32(smem + stage * C::STAGE_BYTES);
+                    const uint32_t s_base = smem_u32(smem + stage * C::STAGE_BYTES);
                     if (pre > 0) {
                         --pre;  // first use of this stage: its weights went out before the wait
                     } else {
@@ -199,15 +207,19 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(fb, C::W_BYTES + nxb * kDecXBoxRows * 128);
-                        tma_load_2d(w_dst, &tmW, 0, (wblk + kb) * 128, fb);
-                        if (GATED) tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb) * 128, fb);
+                        mbar_arrive_expect_tx(fb, nk * (C::W_BYTES + nxb * kDecXBoxRows * 128));
+                        for (int i = 0; i < nk; ++i) {
+                            const uint32_t w_dst = s_base + i * C::W_BYTES;
+                            tma_load_2d(w_dst, &tmW, 0, (wblk + kb + i) * 128, fb);
+                            if (GATED) tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb + i) * 128, fb);
+                        }
                     }
                     // only the boxes that hold rows of this tile; the MMA reads stale shared
                     // memory for the other token columns, whose results are never stored
-                    for (int b = 0; b < nxb; ++b)
-                        tma_load_2d(w_dst + C::W_BYTES + b * kDecXBoxRows * 128, &tmX, kb * 128,
-                                    ti.row0 + b * kDecXBoxRows, fb);
+                    for (int i = 0; i < nk; ++i)
+                        for (int b = 0; b < nxb; ++b)
+                            tma_load_2d(s_base + C::KPS * C::W_BYTES + i * C::X_BYTES + b * kDecXBoxRows * 128, &tmX,
+                                        (kb + i) * 128, ti.row0 + b * kDecXBoxRows, fb);
                     filled |= 1u << stage;
                     if (++stage == nst) {
                         stage = 0;
@@ -238,33 +250,42 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
             uint32_t sphase = 0, tphase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                for (int kb = 0; kb < p.KB; ++kb) {
-                    if (!mbar_wait(smem_u32(&full_bar[stage]), sphase, abort_p, err, kErrTimeoutMma) ||
-                        !mbar_wait(smem_u32(&tempty_bar[buf]), tphase ^ 1u, abort_p, err, kErrTimeoutMma)) {
+                for (int kb = 0; kb < p.KB && ok; kb += C::KPS) {
+                    const int nk = min(C::KPS, p.KB - kb);
+                    if (!mbar_wait(smem_u32(&full_bar[stage]), sphase, abort_p, err, kErrTimeoutMma)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t w_base = smem_u32(smem + stage * C::STAGE_BYTES);
-                    const uint32_t x_base = w_base + C::W_BYTES;
-                    const uint32_t d = tmem_base + (uint32_t)(buf * C::ACC_COLS);
+                    const uint32_t s_base = smem_u32(smem + stage * C::STAGE_BYTES);
+                    // each K block of the stage into its own TMEM buffer (promoted separately)
+                    for (int i = 0; i < nk; ++i) {
+                        if (!mbar_wait(smem_u32(&tempty_bar[buf]), tphase ^ 1u, abort_p, err, kErrTimeoutMma)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t w_base = s_base + i * C::W_BYTES;
+                        const uint32_t x_base = s_base + C::KPS * C::W_BYTES + i * C::X_BYTES;
+                        const uint32_t d = tmem_base + (uint32_t)(buf * C::ACC_COLS);
 #pragma unroll
-                    for (int k4 = 0; k4 < 4; ++k4) {
-                        const uint64_t xd = smem_desc_sw128(x_base + 32 * k4);
-                        mma_e4m3(d, smem_desc_sw128(w_base + 32 * k4), xd, C::IDESC, k4 > 0 ? 1u : 0u);
-                        if (GATED)
-                            mma_e4m3(d + C::BT, smem_desc_sw128(w_base + 128 * 128 + 32 * k4), xd, C::IDESC,
-                                     k4 > 0 ? 1u : 0u);
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const uint64_t xd = smem_desc_sw128(x_base + 32 * k4);
+                            mma_e4m3(d, smem_desc_sw128(w_base + 32 * k4), xd, C::IDESC, k4 > 0 ? 1u : 0u);
+                            if (GATED)
+                                mma_e4m3(d + C::BT, smem_desc_sw128(w_base + 128 * 128 + 32 * k4), xd, C::IDESC,
+                                         k4 > 0 ? 1u : 0u);
+                        }
+                        mma_commit(smem_u32(&tfull_bar[buf]));
+                        if (++buf == C::NBUF) {
+                            buf = 0;
+                            tphase ^= 1u;
+                        }
                     }
+                    if (!ok) break;
                     mma_commit(smem_u32(&empty_bar[stage]));
-                    mma_commit(smem_u32(&tfull_bar[buf]));
                     if (++stage == nst) {
                         stage = 0;
                         sphase ^= 1u;
-                    }
-                    if (++buf == C::NBUF) {
-                        buf = 0;
-                        tphase ^= 1u;
                     }
                 }
             }

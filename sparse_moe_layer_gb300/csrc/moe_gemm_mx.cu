@@ -415,14 +415,18 @@ struct MxDecCfg {
     static constexpr int BT = 32;  // token rows per tile (MMA N)
     static constexpr int W_BYTES = (GATED ? 2 : 1) * 128 * 128;
     static constexpr int X_BYTES = BT * 128;
-    static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
+    // K blocks per ring stage (the ring's round trip is paid once per stage);
+    // a stage holds the KPS weight blocks, then the KPS token-row blocks
+    static constexpr int KPS = GATED ? MOE_MX_DEC_KPS_GATEUP : MOE_MX_DEC_KPS_DOWN;
+    static constexpr int STAGE_BYTES = KPS * (W_BYTES + X_BYTES);
     static constexpr int W_TX = FP4W ? W_BYTES / 2 : W_BYTES;  // packed bytes of 4-bit weight boxes
-    static constexpr int SF_BYTES = (GATED ? 3 : 2) * kMxAtomBytes;  // weight block(s), token tile
-    static constexpr int MAX_STAGES = 16;
+    static constexpr int SF_KB = (GATED ? 3 : 2) * kMxAtomBytes;  // atoms of one K block: weight block(s), token tile
+    static constexpr int SF_BYTES = KPS * SF_KB;
+    static constexpr int MAX_STAGES = 16 / KPS;
     static constexpr int ACC_COLS = GATED ? 2 * BT : BT;
     static constexpr int NACC = 4;  // accumulator buffers
     static constexpr int SF_COL0 = 256;
-    static constexpr int SF_STRIDE = 16;
+    static constexpr int SF_STRIDE = 16 * KPS;  // TMEM scale columns of one stage (16 per K block)
     static constexpr int TMEM_COLS = 512;
     static constexpr int EPI_WARPS = 4;
     static constexpr int META_WARP = 6;
@@ -508,29 +512,34 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, FP4W>::THREADS, 1)
                 const int wblk = (ti.e * p.sw_rowblocks + ti.nt) * p.KB;
                 const int nxb = (ti.rows + kDecXBoxRows - 1) / kDecXBoxRows;
                 const uint8_t* sa = p.sa + (size_t)mtid * p.KB * kMxAtomBytes;
-                for (int kb = 0; kb < p.KB; ++kb) {
+                for (int kb0 = 0; kb0 < p.KB; kb0 += C::KPS) {
+                    const int nk = min(C::KPS, p.KB - kb0);
                     if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_p, err, kErrTimeoutProducer)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = smem_u32(&full_bar[stage]);
-                    mbar_arrive_expect_tx(fb, C::W_TX + nxb * kDecXBoxRows * 128 + C::SF_BYTES);
-                    const uint32_t w_dst = smem_u32(smem + stage * C::STAGE_BYTES);
-                    const uint32_t sf_dst = smem_u32(sf_smem + stage * C::SF_BYTES);
-                    tma_load_2d(w_dst, &tmW, 0, (wblk + kb) * 128, fb);
-                    bulk_load(sf_dst, p.sw + (size_t)(wblk + kb) * kMxAtomBytes, kMxAtomBytes, fb);
-                    if (GATED) {
-                        tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb) * 128, fb);
-                        bulk_load(sf_dst + kMxAtomBytes, p.sw + (size_t)(wblk + ublk + kb) * kMxAtomBytes,
+                    mbar_arrive_expect_tx(fb, nk * (C::W_TX + nxb * kDecXBoxRows * 128 + C::SF_KB));
+                    for (int i = 0; i < nk; ++i) {
+                        const int kb = kb0 + i;
+                        const uint32_t w_dst = smem_u32(smem + stage * C::STAGE_BYTES + i * C::W_BYTES);
+                        const uint32_t x_dst = smem_u32(smem + stage * C::STAGE_BYTES + C::KPS * C::W_BYTES +
+                                                        i * C::X_BYTES);
+                        const uint32_t sf_dst = smem_u32(sf_smem + stage * C::SF_BYTES + i * C::SF_KB);
+                        tma_load_2d(w_dst, &tmW, 0, (wblk + kb) * 128, fb);
+                        bulk_load(sf_dst, p.sw + (size_t)(wblk + kb) * kMxAtomBytes, kMxAtomBytes, fb);
+                        if (GATED) {
+                            tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb) * 128, fb);
+                            bulk_load(sf_dst + kMxAtomBytes, p.sw + (size_t)(wblk + ublk + kb) * kMxAtomBytes,
+                                      kMxAtomBytes, fb);
+                        }
+                        // only the boxes that hold rows of this tile; the MMA reads stale shared
+                        // memory for the other token columns, whose results are never stored
+                        for (int b = 0; b < nxb; ++b)
+                            tma_load_2d(x_dst + b * kDecXBoxRows * 128, &tmX, kb * 128, ti.row0 + b * kDecXBoxRows, fb);
+                        bulk_load(sf_dst + (GATED ? 2 : 1) * kMxAtomBytes, sa + (size_t)kb * kMxAtomBytes,
                                   kMxAtomBytes, fb);
                     }
-                    // only the boxes that hold rows of this tile; the MMA reads stale shared
-                    // memory for the other token columns, whose results are never stored
-                    for (int b = 0; b < nxb; ++b)
-                        tma_load_2d(w_dst + C::W_BYTES + b * kDecXBoxRows * 128, &tmX, kb * 128,
-                                    ti.row0 + b * kDecXBoxRows, fb);
-                    bulk_load(sf_dst + (GATED ? 2 : 1) * kMxAtomBytes, sa + (size_t)kb * kMxAtomBytes, kMxAtomBytes,
-                              fb);
                     filled |= 1u << stage;
                     if (++stage == nst) {
                         stage = 0;
@@ -564,29 +573,34 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, FP4W>::THREADS, 1)
                 if (!mbar_wait(smem_u32(&dempty_bar[buf]), aphase ^ 1u, abort_p, err, kErrTimeoutMma)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(buf * C::ACC_COLS);
-                for (int kb = 0; kb < p.KB; ++kb) {
+                for (int kb0 = 0; kb0 < p.KB; kb0 += C::KPS) {
+                    const int nk = min(C::KPS, p.KB - kb0);
                     if (!mbar_wait(smem_u32(&full_bar[stage]), sphase, abort_p, err, kErrTimeoutMma)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t w_base = smem_u32(smem + stage * C::STAGE_BYTES);
-                    const uint32_t x_base = w_base + C::W_BYTES;
-                    const uint32_t sf_src = smem_u32(sf_smem + stage * C::SF_BYTES);
-                    const uint32_t tsf = tmem_base + (uint32_t)(C::SF_COL0 + stage * C::SF_STRIDE);
-                    // SFA: gate (or only) block [tsf, tsf+4), up block [tsf+4, tsf+8); SFB: tokens [tsf+8, ...)
-                    tmem_cp_atom(tsf, sf_src);
-                    if (GATED) tmem_cp_atom(tsf + 4, sf_src + kMxAtomBytes);
-                    tmem_cp_atom(tsf + 8, sf_src + (GATED ? 2 : 1) * kMxAtomBytes);
+                    for (int i = 0; i < nk; ++i) {
+                        const int kb = kb0 + i;
+                        const uint32_t w_base = smem_u32(smem + stage * C::STAGE_BYTES + i * C::W_BYTES);
+                        const uint32_t x_base = smem_u32(smem + stage * C::STAGE_BYTES + C::KPS * C::W_BYTES +
+                                                         i * C::X_BYTES);
+                        const uint32_t sf_src = smem_u32(sf_smem + stage * C::SF_BYTES + i * C::SF_KB);
+                        const uint32_t tsf = tmem_base + (uint32_t)(C::SF_COL0 + stage * C::SF_STRIDE + 16 * i);
+                        // SFA: gate (or only) block [tsf, tsf+4), up block [tsf+4, tsf+8); SFB: tokens [tsf+8, ...)
+                        tmem_cp_atom(tsf, sf_src);
+                        if (GATED) tmem_cp_atom(tsf + 4, sf_src + kMxAtomBytes);
+                        tmem_cp_atom(tsf + 8, sf_src + (GATED ? 2 : 1) * kMxAtomBytes);
 #pragma unroll
-                    for (int k4 = 0; k4 < 4; ++k4) {
-                        const uint64_t xd = smem_desc_sw128(x_base + 32 * k4);
-                        const uint32_t id = idesc_sf_id(C::IDESC, (uint32_t)k4);
-                        const uint32_t acc = (kb | k4) != 0 ? 1u : 0u;
-                        mma_mx(d, smem_desc_sw128(w_base + 32 * k4), xd, id, tsf, tsf + 8, acc);
-                        if (GATED)
-                            mma_mx(d + C::BT, smem_desc_sw128(w_base + 128 * 128 + 32 * k4), xd, id, tsf + 4, tsf + 8,
-                                   acc);
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const uint64_t xd = smem_desc_sw128(x_base + 32 * k4);
+                            const uint32_t id = idesc_sf_id(C::IDESC, (uint32_t)k4);
+                            const uint32_t acc = (kb | k4) != 0 ? 1u : 0u;
+                            mma_mx(d, smem_desc_sw128(w_base + 32 * k4), xd, id, tsf, tsf + 8, acc);
+                            if (GATED)
+                                mma_mx(d + C::BT, smem_desc_sw128(w_base + 128 * 128 + 32 * k4), xd, id, tsf + 4,
+                                       tsf + 8, acc);
+                        }
                     }
                     mma_commit(smem_u32(&empty_bar[stage]));
                     if (++stage == nst) {

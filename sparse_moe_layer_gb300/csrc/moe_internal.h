@@ -61,6 +61,23 @@ constexpr int kDecXBoxRows = 8;  // activation rows per TMA box of the decode GE
 #ifndef MOE_DEC_STAGES_DOWN
 #define MOE_DEC_STAGES_DOWN 9
 #endif
+// K blocks per ring stage of the MX decode GEMMs: the down GEMM (one weight
+// block per K block) runs faster with two per stage (oss120b_decode: MXFP8
+// 209 -> 186 us, MXFP4 210 -> 182 us), the gate/up GEMM slower (326 -> 344,
+// 274 -> 285 us)
+#ifndef MOE_MX_DEC_KPS_GATEUP
+#define MOE_MX_DEC_KPS_GATEUP 1
+#endif
+#ifndef MOE_MX_DEC_KPS_DOWN
+#define MOE_MX_DEC_KPS_DOWN 2
+#endif
+// K blocks per ring stage of the 128x128 decode GEMMs (two were slower for both)
+#ifndef MOE_DEC_KPS_GATEUP
+#define MOE_DEC_KPS_GATEUP 1
+#endif
+#ifndef MOE_DEC_KPS_DOWN
+#define MOE_DEC_KPS_DOWN 1
+#endif
 constexpr int kDecStagesGateUp = MOE_DEC_STAGES_GATEUP;  // stage ring depth of the decode GEMMs (upper bound)
 constexpr int kDecStagesDown = MOE_DEC_STAGES_DOWN;
 
