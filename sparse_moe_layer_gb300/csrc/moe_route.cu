@@ -17,11 +17,11 @@ namespace moe {
 // expert index) are stored in ascending expert order with the softmax over
 // their k logits in fp32 ("softmax after top-k", "softmax only over the
 // selected experts"), rounded to bf16 for the combine ("expert weights in
-// bfloat16").  One kernel (router_kernel, below) computes the logits with a
-// thread-block cluster per 32-token tile and selects; for large batches its
-// last CTA also turns the (chunk, expert) histogram into the per-expert row
-// offsets, per-chunk row bases and GEMM tile lists, for small ones the
-// permutation kernel does that itself.
+// bfloat16").  One kernel computes the logits and selects (router_kernel: a
+// thread-block cluster per token tile; router_tc_kernel: tensor cores, for
+// large batches); the last CTA of either turns the (chunk, expert) histogram
+// into the per-expert row offsets, per-chunk row bases and GEMM tile lists,
+// so those are final when the router grid completes.
 
 // The k largest of lg[0..E) for one warp (ties -> lower index), ascending.
 __device__ __forceinline__ void select_topk(const float* lg, int E, int k, int lane, int* chosen) {
