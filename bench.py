@@ -542,8 +542,10 @@ def main():
     else:
         roof = dict(bound="hbm", achieved=alg["gemm1_bytes"] / g1_s / 1e9, peak=pk["hbm"], unit="GB/s")
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = recorded_traffic("gemm_gateup_mx4" if fp4 else "gemm_gateup_mx" if mx else "gemm_gateup",
-                                       cfg.name, mx, decode=not prefill)
+    # a record holds for the named workload itself, not for a --tokens / --routing variant of it
+    own_workload = args.tokens == 0 and args.routing == "synthetic"
+    roof["traffic"] = (recorded_traffic("gemm_gateup_mx4" if fp4 else "gemm_gateup_mx" if mx else "gemm_gateup",
+                                        cfg.name, mx, decode=not prefill) if own_workload else None)
     if fp4:
         roof["kernel"] = ("moe_gemm_mx_kernel<true, FP4W> (block-scaled e4m3 x e2m1 gate/up GEMM + SwiGLU + MX "
                           "requant)" if prefill else
