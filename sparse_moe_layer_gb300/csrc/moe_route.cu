@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "moe_device.cuh"
 #include "moe_internal.h"
 
@@ -165,13 +167,20 @@ __device__ void finish_scan(const RouteParams& p, int* buf, int cap) {
 }
 
 // True in every thread of the CTA that is the `total`-th to arrive on *ctr.
+// The barrier orders every thread's earlier writes before thread 0's
+// GPU-scope fence, which (fences are cumulative) orders them before its
+// count; in the last CTA thread 0 fences again after the count, and the
+// barrier behind it orders the other threads' reads after that.
 __device__ __forceinline__ bool last_to_arrive(int* ctr, int total) {
     __shared__ int s_last;
-    __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_last = (atomicAdd(ctr, 1) == total - 1);
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const bool last = atomicAdd(ctr, 1) == total - 1;
+        if (last) __threadfence();
+        s_last = last;
+    }
     __syncthreads();
-    if (s_last) __threadfence();
     return s_last != 0;
 }
 
@@ -184,8 +193,8 @@ __device__ __forceinline__ bool last_to_arrive(int* ctr, int total) {
 // The KS partial tiles are then summed in rank order through distributed
 // shared memory (the same order whatever CTA sums), each CTA finishing the
 // tokens r, r + KS, ...: bias, top-k and softmax for one token per warp.  So
-// small batches spread over up to 8x more SMs than they have token tiles, and
-// no partial logit goes through global memory.
+// small batches spread over up to 8x (16x with at most 64 experts) more SMs
+// than they have token tiles, and no partial logit goes through global memory.
 constexpr int kRtTok = 32;      // tokens per cluster, decode-sized batches
 constexpr int kRtTokBig = 128;  // tokens per cluster, large batches (64 beyond 128 experts)
 constexpr int kRtBigT = 2048;   // batches of at least this many tokens take the large tile
@@ -351,14 +360,50 @@ static cudaError_t launch_router_t(const RouteParams& p, cudaStream_t st) {
     // about two CTAs per SM in all with the small tile; one (shared memory)
     // with the large one
     const int want = TOK == kRtTok ? 296 : 152;
-    int ks = ntiles >= want / 2 ? 1 : want / ntiles;
-    ks = ks < 1 ? 1 : (ks > 8 ? 8 : ks);
-    if (ks > nchunk) ks = nchunk;
-    const int cpc = (nchunk + ks - 1) / ks;
-    ks = (nchunk + cpc - 1) / cpc;  // no CTA without a chunk
+    // Up to 16 CTAs per cluster (a non-portable size) with at most 64 experts:
+    // fewer K chunks per CTA shortened the router of a 64-token, 32-expert,
+    // 2880-wide batch from 17.0-17.4 to 15.6-16.1 us, while 128 experts (a
+    // longer rank-order sum per logit) gained nothing; 8 elsewhere, or where
+    // this device cannot co-schedule 16.
+    static std::atomic<int> wide_ok{-1};
     cudaError_t e = cudaFuncSetAttribute(router_kernel<NTW, VEC, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::SMEM);
     if (e != cudaSuccess) return e;
+    // function attributes belong to the current device's context: set on every launch
+    const bool wide_attr =
+        NTW == 1 &&
+        cudaFuncSetAttribute(router_kernel<NTW, VEC, TOK>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess;
+    if (!wide_attr) (void)cudaGetLastError();
+    if (wide_attr && wide_ok.load() < 0) {
+        int ok = 0;
+        {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(16);
+            q.blockDim = dim3(256);
+            q.dynamicSmemBytes = C::SMEM;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = 16;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            q.attrs = qa;
+            q.numAttrs = 1;
+            int nclusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&nclusters, router_kernel<NTW, VEC, TOK>, &q) == cudaSuccess &&
+                nclusters > 0)
+                ok = 1;
+            else
+                (void)cudaGetLastError();
+        }
+        wide_ok.store(ok);
+    }
+    const int ks_max = wide_attr && wide_ok.load() == 1 ? 16 : 8;
+    int ks = ntiles >= want / 2 ? 1 : want / ntiles;
+    ks = ks < 1 ? 1 : (ks > ks_max ? ks_max : ks);
+    if (ks > nchunk) ks = nchunk;
+    const int cpc = (nchunk + ks - 1) / ks;
+    ks = (nchunk + cpc - 1) / cpc;  // no CTA without a chunk
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ntiles * ks);
     cfg.blockDim = dim3(256);
