@@ -366,7 +366,12 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     const bool decode = decode_sized(R, E);
     const int bm = decode ? 32 : 128;
     const int nt1 = Ip / 128;
-    const int nt2 = decode ? Hp / 128 : (Hp / 128 + 1) / 2;
+    // The decode down GEMM takes two w2 row blocks per tile, half the row
+    // blocks apart (two weight streams per K step, as the gate/up GEMM has),
+    // unless one-block tiles would not even fill the SMs: min(E, R) experts
+    // can be active.
+    const bool pair_down = decode && !mx && (long long)(E < R ? E : R) * (Hp / 128) > sms;
+    const int nt2 = decode && !pair_down ? Hp / 128 : (Hp / 128 + 1) / 2;
     RoutingBuffers rb;
     rb.status = reinterpret_cast<uint32_t*>(ws + L.status);
     rb.zero_bytes = L.count - L.status;
@@ -489,7 +494,7 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     g2.KB = Ip / 128;
     g2.N_real = H;
     g2.rows_B = Hp;
-    g2.up_rows = 0;
+    g2.up_rows = pair_down ? nt2 * 128 : 0;  // tile nt: w2 row blocks nt and nt + nt2
     g2.sw_rowblocks = Hp / 128;
     g2.count = rb.count;
     g2.offset = rb.offset;

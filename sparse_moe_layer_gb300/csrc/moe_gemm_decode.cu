@@ -8,14 +8,21 @@
 // by streaming the activated experts' weights from HBM ("Hosting Qwen on
 // Blackwell", Decoders: with few tokens the GEMM is limited by loading
 // weights into the tensor cores), so nearly all of every pipeline stage is
-// weight bytes: 5 stages of 32 KB (gate + up) or 9 of 16 KB (down) are in
-// flight per SM -- deeper rings were measured and gain nothing -- and the
-// small TMEM tiles give 8-16 accumulation buffers, so the scale promotion
-// never stalls the MMA.  A tile loads only the 8-row boxes of token rows it
-// has; the metadata slots are sized by the K-block count.
+// weight bytes: 5 stages of two 16 KB weight blocks are in flight per SM --
+// deeper rings were measured and gain nothing -- and the small TMEM tiles
+// give 8-16 accumulation buffers, so the scale promotion never stalls the
+// MMA.  A tile loads only the 8-row boxes of token rows it has; the metadata
+// slots are sized by the K-block count.
 //
-// Tile = (expert, 128 output features, 32 token rows), ordered expert,
-// n-tile, m-tile; one CTA per SM, persistent.
+// Tile = (expert, 128 output features -- 256 for the gate/up GEMM's gate and
+// up halves and for the paired down GEMM -- and 32 token rows), ordered
+// expert, n-tile, m-tile; one CTA per SM, persistent.  Two weight blocks per
+// K step stream faster than one: with one 16 KB block per stage the down
+// GEMM's stages arrived every ~0.48 us whatever the ring depth (9 or 5
+// stages), with two every ~0.75 us.  So the down GEMM pairs w2 row blocks nt
+// and nt + ceil(RB/2) in one tile, except when one-block tiles would not
+// fill the SMs (a batch of one token), where twice the tiles win.
+//
 //   warp 0     TMA producer (weights: one or two 128x128 boxes; tokens: the
 //              tile's rows in boxes of 8)
 //   warp 1     TMEM allocator and MMA issuer
@@ -35,10 +42,14 @@
 
 namespace moe {
 
-template <bool GATED>
+// GATED: the gate/up GEMM (gate and up row blocks of one n-tile per K step).
+// PAIRED (down GEMM only): two w2 row blocks per K step, nt and nt + U with
+// U = ceil(row blocks / 2), 256 output features per tile.
+template <bool GATED, bool PAIRED = false>
 struct DecCfg {
+    static constexpr bool TWO = GATED || PAIRED;          // two weight row blocks per K step
     static constexpr int BT = 32;                         // token rows per tile (MMA N)
-    static constexpr int W_BYTES = (GATED ? 2 : 1) * 128 * 128;
+    static constexpr int W_BYTES = (TWO ? 2 : 1) * 128 * 128;
     static constexpr int X_BYTES = BT * 128;
     // K blocks per ring stage (one: two per stage were measured slower for both
     // GEMMs, which stream at their bound with one)
@@ -46,9 +57,9 @@ struct DecCfg {
     // stage: the KPS weight blocks, then the KPS token-row blocks
     static constexpr int STAGE_BYTES = KPS * (W_BYTES + X_BYTES);
     static constexpr int MAX_STAGES = 16;                 // the ring takes what shared memory is left (launch)
-    static constexpr int ACC_COLS = GATED ? 2 * BT : BT;  // TMEM columns of one accumulation buffer
+    static constexpr int ACC_COLS = TWO ? 2 * BT : BT;    // TMEM columns of one accumulation buffer
     static constexpr int TMEM_COLS = 512;
-    static constexpr int NBUF = TMEM_COLS / ACC_COLS;     // 8 (gate/up) or 16 (down)
+    static constexpr int NBUF = TMEM_COLS / ACC_COLS;     // 8 (two row blocks) or 16
     static constexpr int EPI_WARPS = 4;
     static constexpr int META_WARP = 6;
     static constexpr int THREADS = 7 * 32;
@@ -97,11 +108,20 @@ __device__ __forceinline__ DecTile decode_dec_tile(int tile, const int* s_tiles,
     return ti;
 }
 
-template <bool GATED>
-__global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
+// Whether a tile has a second weight row block, up_rows / 128 row blocks
+// past its first (block (e, row block, kb) starts at row ((e*RB + rb)*KB +
+// kb)*128): always for gate/up (the up half); for a paired down tile unless
+// that is past the last w2 row block.
+template <bool GATED, bool PAIRED>
+__device__ __forceinline__ bool dec_has_second(const DecTile& ti, const GemmParams& p) {
+    return GATED || (PAIRED && ti.nt + p.up_rows / 128 < p.sw_rowblocks);
+}
+
+template <bool GATED, bool PAIRED>
+__global__ void __launch_bounds__(DecCfg<GATED, PAIRED>::THREADS, 1)
     moe_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                            const GemmParams p, const int nst) {
-    using C = DecCfg<GATED>;
+    using C = DecCfg<GATED, PAIRED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const DecMeta M = dec_meta(p.KB);
@@ -167,16 +187,17 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
         for (int tile = blockIdx.x; tile < total && pre < nst; tile += gridDim.x) {
             const DecTile ti = decode_dec_tile(tile, s_tiles, s_off, s_cnt, E);
             const int wblk = (ti.e * p.sw_rowblocks + ti.nt) * p.KB;
-            const int ublk = GATED ? (p.up_rows / 128) * p.KB : 0;
+            const int ublk = (p.up_rows / 128) * p.KB;
+            const bool two = dec_has_second<GATED, PAIRED>(ti, p);
             const int nxb = (ti.rows + kDecXBoxRows - 1) / kDecXBoxRows;
             for (int kb = 0; kb < p.KB && pre < nst; kb += C::KPS, ++pre) {
                 const int nk = min(C::KPS, p.KB - kb);
                 const uint32_t fb = smem_u32(&full_bar[pre]);
-                mbar_arrive_expect_tx(fb, nk * (C::W_BYTES + nxb * kDecXBoxRows * 128));
+                mbar_arrive_expect_tx(fb, nk * ((two ? 2 : 1) * 128 * 128 + nxb * kDecXBoxRows * 128));
                 for (int i = 0; i < nk; ++i) {
                     const uint32_t w_dst = smem_u32(smem + pre * C::STAGE_BYTES + i * C::W_BYTES);
                     tma_load_2d(w_dst, &tmW, 0, (wblk + kb + i) * 128, fb);
-                    if (GATED) tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb + i) * 128, fb);
+                    if (C::TWO && two) tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb + i) * 128, fb);
                 }
             }
         }
@@ -192,9 +213,9 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const DecTile ti = decode_dec_tile(tile, s_tiles, s_off, s_cnt, E);
-                // blocked weights: block (e, row block, kb) starts at row ((e*RB + rb)*KB + kb)*128
                 const int wblk = (ti.e * p.sw_rowblocks + ti.nt) * p.KB;
-                const int ublk = GATED ? (p.up_rows / 128) * p.KB : 0;
+                const int ublk = (p.up_rows / 128) * p.KB;
+                const bool two = dec_has_second<GATED, PAIRED>(ti, p);
                 const int nxb = (ti.rows + kDecXBoxRows - 1) / kDecXBoxRows;
                 for (int kb = 0; kb < p.KB; kb += C::KPS) {
                     const int nk = min(C::KPS, p.KB - kb);
@@ -207,11 +228,12 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(fb, nk * (C::W_BYTES + nxb * kDecXBoxRows * 128));
+                        mbar_arrive_expect_tx(fb, nk * ((two ? 2 : 1) * 128 * 128 + nxb * kDecXBoxRows * 128));
                         for (int i = 0; i < nk; ++i) {
                             const uint32_t w_dst = s_base + i * C::W_BYTES;
                             tma_load_2d(w_dst, &tmW, 0, (wblk + kb + i) * 128, fb);
-                            if (GATED) tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb + i) * 128, fb);
+                            if (C::TWO && two)
+                                tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb + i) * 128, fb);
                         }
                     }
                     // only the boxes that hold rows of this tile; the MMA reads stale shared
@@ -250,6 +272,8 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
             uint32_t sphase = 0, tphase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const bool two = C::TWO && dec_has_second<GATED, PAIRED>(
+                                               decode_dec_tile(tile, s_tiles, s_off, s_cnt, E), p);
                 for (int kb = 0; kb < p.KB && ok; kb += C::KPS) {
                     const int nk = min(C::KPS, p.KB - kb);
                     if (!mbar_wait(smem_u32(&full_bar[stage]), sphase, abort_p, err, kErrTimeoutMma)) {
@@ -271,7 +295,7 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                         for (int k4 = 0; k4 < 4; ++k4) {
                             const uint64_t xd = smem_desc_sw128(x_base + 32 * k4);
                             mma_e4m3(d, smem_desc_sw128(w_base + 32 * k4), xd, C::IDESC, k4 > 0 ? 1u : 0u);
-                            if (GATED)
+                            if (two)
                                 mma_e4m3(d + C::BT, smem_desc_sw128(w_base + 128 * 128 + 32 * k4), xd, C::IDESC,
                                          k4 > 0 ? 1u : 0u);
                         }
@@ -302,11 +326,13 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
             if (!mbar_wait(smem_u32(&mempty_bar[slot]), use ^ 1u, abort_p, err, kErrTimeoutProducer)) break;
             float* m = meta + slot * M.floats;
             const DecTile ti = decode_dec_tile(tile, s_tiles, s_off, s_cnt, E);
+            const bool two = dec_has_second<GATED, PAIRED>(ti, p);
             const uint16_t* bias_e = p.bias + (size_t)ti.e * (GATED ? 2 * p.N_real : p.N_real);
+            // bias of the tile's features: [0, 128) first row block, [128, 256) second
 #pragma unroll
-            for (int c = lane; c < (GATED ? 256 : 128); c += 32) {
-                const int n = ti.nt * 128 + (c & 127);
-                m[c] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + (c >> 7) * p.N_real + n)) : 0.f;
+            for (int c = lane; c < (C::TWO ? 256 : 128); c += 32) {
+                const int n = ti.nt * 128 + (c & 127) + (GATED ? 0 : (c >> 7) * p.up_rows);
+                m[c] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + (GATED ? (c >> 7) * p.N_real : 0) + n)) : 0.f;
             }
             const int rtok = min(ti.row0 + lane, p.R - 1);
             // the tile's token scales, eight K blocks in flight per lane
@@ -321,7 +347,7 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
             const float* sw_g = p.sw + ((size_t)ti.e * p.sw_rowblocks + ti.nt) * p.KB;
             for (int kb = lane; kb < p.KB; kb += 32) {
                 m[M.sw + kb] = __ldg(sw_g + kb);
-                if (GATED) m[M.swu + kb] = __ldg(sw_g + (p.up_rows / 128) * p.KB + kb);
+                if (C::TWO) m[M.swu + kb] = two ? __ldg(sw_g + (p.up_rows / 128) * p.KB + kb) : 0.f;
             }
             if (!GATED) {
                 const int slot_t = __ldg(p.perm + rtok);
@@ -350,11 +376,11 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
             float acc[C::ACC_COLS];
             {
                 const float bg = m[nl];
-                const float bu = GATED ? m[128 + nl] : 0.f;
+                const float bu = C::TWO ? m[128 + nl] : 0.f;
 #pragma unroll
                 for (int j = 0; j < C::BT; ++j) {
                     acc[j] = bg;
-                    if (GATED) acc[C::BT + j] = bu;
+                    if (C::TWO) acc[C::BT + j] = bu;
                 }
             }
             for (int kb = 0; kb < p.KB; ++kb) {
@@ -366,7 +392,7 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                 const uint32_t tcol = t_lane + (uint32_t)(buf * C::ACC_COLS);
                 const float a = m[M.sa + kb * 32 + lane];  // lane j: scale of token j in this K block
                 const float fg = a * m[M.sw + kb];
-                if (GATED) {
+                if (C::TWO) {
                     const float fu = a * m[M.swu + kb];
                     uint32_t r[64];
                     tmem_ld64(tcol, r);
@@ -431,11 +457,15 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
                 const int slot_l = reinterpret_cast<const int*>(m)[M.slot + lane];
                 const float w_l = m[M.w + lane];
                 mbar_arrive(smem_u32(&mempty_bar[slot]));
+                const bool two = dec_has_second<GATED, PAIRED>(ti, p);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int slot_t = __shfl_sync(0xffffffffu, slot_l, j);
                     const float w = __shfl_sync(0xffffffffu, w_l, j);
-                    if (j < ti.rows) p.part[(size_t)slot_t * p.ldp + n] = w * acc[j];
+                    if (j < ti.rows) {
+                        p.part[(size_t)slot_t * p.ldp + n] = w * acc[j];
+                        if (C::TWO && two) p.part[(size_t)slot_t * p.ldp + n + p.up_rows] = w * acc[C::BT + j];
+                    }
                 }
             }
         }
@@ -451,15 +481,15 @@ __global__ void __launch_bounds__(DecCfg<GATED>::THREADS, 1)
 
 // The stage ring takes the shared memory the metadata slots and the kernel's
 // static arrays leave, up to `max_stages` stages.
-template <bool GATED>
+template <bool GATED, bool PAIRED>
 static cudaError_t launch_dec(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int grid,
                               int max_stages, cudaStream_t st) {
-    using C = DecCfg<GATED>;
+    using C = DecCfg<GATED, PAIRED>;
     int dev = 0, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     cudaFuncAttributes fa;
-    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, moe_gemm_decode_kernel<GATED>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, moe_gemm_decode_kernel<GATED, PAIRED>);
     if (e != cudaSuccess) return e;
     const size_t meta = (size_t)2 * dec_meta(p.KB).floats * 4;
     const long long room = (long long)optin - (long long)fa.sharedSizeBytes - 1024 - (long long)meta;
@@ -468,19 +498,22 @@ static cudaError_t launch_dec(const CUtensorMap& tmW, const CUtensorMap& tmX, co
     if (nst > C::MAX_STAGES) nst = C::MAX_STAGES;
     if (nst < 2) return cudaErrorInvalidConfiguration;
     const size_t smem = (size_t)nst * C::STAGE_BYTES + meta + 1024;
-    e = cudaFuncSetAttribute(moe_gemm_decode_kernel<GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(moe_gemm_decode_kernel<GATED, PAIRED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(moe_gemm_decode_kernel<GATED>, dim3(grid), dim3(C::THREADS), smem, st, tmW, tmX, p, nst);
+    return launch_pdl(moe_gemm_decode_kernel<GATED, PAIRED>, dim3(grid), dim3(C::THREADS), smem, st, tmW, tmX, p, nst);
 }
 
 cudaError_t launch_gemm_gateup_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int grid,
                                       cudaStream_t st) {
-    return launch_dec<true>(tmW, tmX, p, grid, kDecStagesGateUp, st);
+    return launch_dec<true, false>(tmW, tmX, p, grid, kDecStagesGateUp, st);
 }
 
 cudaError_t launch_gemm_down_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int grid,
                                     cudaStream_t st) {
-    return launch_dec<false>(tmW, tmX, p, grid, kDecStagesDown, st);
+    // up_rows != 0: tiles of two w2 row blocks (the tile list was counted with
+    // ceil(row blocks / 2) n-tiles per m-tile)
+    return p.up_rows != 0 ? launch_dec<false, true>(tmW, tmX, p, grid, kDecStagesGateUp, st)
+                          : launch_dec<false, false>(tmW, tmX, p, grid, kDecStagesDown, st);
 }
 
 }  // namespace moe

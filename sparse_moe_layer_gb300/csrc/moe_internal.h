@@ -85,7 +85,8 @@ struct GemmParams {
     int E, R, KB;          // K / 128
     int N_real;            // gate/up GEMM: I; down GEMM: H
     int rows_B;            // rows of one expert's weight matrix: 2*Ip or Hp
-    int up_rows;           // gate/up GEMM: Ip (row offset of the up half)
+    int up_rows;           // rows from a tile's first weight row block to its second: gate/up GEMM Ip
+                           // (the up half); paired decode down GEMM ceil(Hp/256)*128; else 0
     int sw_rowblocks;      // rows_B / 128
     const int32_t* count;
     const int32_t* offset;
