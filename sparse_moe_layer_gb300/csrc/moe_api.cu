@@ -236,6 +236,18 @@ static moe_status launch_routing(const void* x, const void* router_w, const void
     return MOE_OK;
 }
 
+// How many n-tiles of each m-tile the decode down GEMM gives two w2 row
+// blocks (j and j + P, j < P); the other RB - 2P take one, listed after all
+// the paired tiles.  Two blocks per K step stream faster per byte than one
+// (per K block ~0.75 us against ~0.48 us for one with 128x128 block scales),
+// so every block that can be paired is, unless one-block tiles for the
+// `active` experts that can have rows would not even fill the SMs.  (Fewer
+// pairs, to even out the tiles per CTA, measured slower: one-block tiles in
+// the paired kernel are no cheaper per byte.)
+static int decode_down_pairs(int RB, int active, int sms) {
+    return (long long)active * RB > sms ? RB / 2 : 0;
+}
+
 // Launch sequence shared by moe_forward and moe_forward_profiled; when `ev`
 // is non-null, ev[i] is recorded on the stream before stage i and ev[5]
 // after the last stage.
@@ -366,12 +378,10 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     const bool decode = decode_sized(R, E);
     const int bm = decode ? 32 : 128;
     const int nt1 = Ip / 128;
-    // The decode down GEMM takes two w2 row blocks per tile, half the row
-    // blocks apart (two weight streams per K step, as the gate/up GEMM has),
-    // unless one-block tiles would not even fill the SMs: min(E, R) experts
-    // can be active.
-    const bool pair_down = decode && !mx && (long long)(E < R ? E : R) * (Hp / 128) > sms;
-    const int nt2 = decode && !pair_down ? Hp / 128 : (Hp / 128 + 1) / 2;
+    // Decode down GEMM: the first `pairs` n-tiles of every m-tile take two w2
+    // row blocks, the rest one (decode_down_pairs).
+    const int pairs = decode ? decode_down_pairs(Hp / 128, E < R ? E : R, sms) : 0;
+    const int nt2 = decode ? Hp / 128 - pairs : (Hp / 128 + 1) / 2;
     RoutingBuffers rb;
     rb.status = reinterpret_cast<uint32_t*>(ws + L.status);
     rb.zero_bytes = L.count - L.status;
@@ -439,6 +449,7 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
         m2.KB = Ip / 128;
         m2.N_real = H;
         m2.sw_rowblocks = Hp / 128;
+        m2.up_rows = pairs * 128;  // paired tile j < pairs: w2 row blocks j and j + pairs
         m2.nt = nt2;
         m2.count = rb.count;
         m2.offset = rb.offset;
@@ -494,7 +505,7 @@ static moe_status forward_impl(const void* x, const void* router_w, const void* 
     g2.KB = Ip / 128;
     g2.N_real = H;
     g2.rows_B = Hp;
-    g2.up_rows = pair_down ? nt2 * 128 : 0;  // tile nt: w2 row blocks nt and nt + nt2
+    g2.up_rows = pairs * 128;  // paired tile j < pairs: w2 row blocks j and j + pairs
     g2.sw_rowblocks = Hp / 128;
     g2.count = rb.count;
     g2.offset = rb.offset;

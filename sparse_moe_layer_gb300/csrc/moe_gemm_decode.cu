@@ -19,9 +19,10 @@
 // expert, n-tile, m-tile; one CTA per SM, persistent.  Two weight blocks per
 // K step stream faster than one: with one 16 KB block per stage the down
 // GEMM's stages arrived every ~0.48 us whatever the ring depth (9 or 5
-// stages), with two every ~0.75 us.  So the down GEMM pairs w2 row blocks nt
-// and nt + ceil(RB/2) in one tile, except when one-block tiles would not
-// fill the SMs (a batch of one token), where twice the tiles win.
+// stages), with two every ~0.75 us.  So the down GEMM pairs w2 row blocks j
+// and j + P in its first P n-tiles, P chosen at launch for the balance of
+// the tile list over the SMs (0 -- one block per tile -- when one-block
+// tiles would not even fill them).
 //
 //   warp 0     TMA producer (weights: one or two 128x128 boxes; tokens: the
 //              tile's rows in boxes of 8)
@@ -66,8 +67,11 @@ struct DecCfg {
     static constexpr uint32_t IDESC = idesc_e4m3_f32(128, BT);
 };
 
+// nt: the tile's (first) weight row block within the expert; two: whether a
+// second row block, up_rows / 128 further on, is part of it
 struct DecTile {
     int e, nt, row0, rows;
+    bool two;
 };
 
 // One metadata slot (floats), sized by the K-block count: bias [256], token
@@ -108,13 +112,49 @@ __device__ __forceinline__ DecTile decode_dec_tile(int tile, const int* s_tiles,
     return ti;
 }
 
-// Whether a tile has a second weight row block, up_rows / 128 row blocks
-// past its first (block (e, row block, kb) starts at row ((e*RB + rb)*KB +
-// kb)*128): always for gate/up (the up half); for a paired down tile unless
-// that is past the last w2 row block.
+// Tile -> (expert, row block(s), m-tile).  Gate/up and one-block down tiles:
+// the list is ordered expert, n-tile, m-tile (decode_dec_tile).  Paired down
+// tiles (P = up_rows / 128 > 0): of the NT = RB - P n-tiles of an m-tile, the
+// first P take w2 row blocks j and j + P, the other RB - 2P one block each
+// (2P .. RB-1); the list holds every m-tile's P paired tiles (m-tile by
+// m-tile, expert order) before all the one-block ones, so that a round-robin
+// assignment gives no CTA more paired tiles than another has plus one.
+// Weight block (e, row block, kb) starts at row ((e*RB + rb)*KB + kb)*128.
 template <bool GATED, bool PAIRED>
-__device__ __forceinline__ bool dec_has_second(const DecTile& ti, const GemmParams& p) {
-    return GATED || (PAIRED && ti.nt + p.up_rows / 128 < p.sw_rowblocks);
+__device__ __forceinline__ DecTile dec_tile(int tile, const int* s_tiles, const int* s_off, const int* s_cnt, int E,
+                                            const GemmParams& p) {
+    if (!PAIRED) {
+        DecTile t = decode_dec_tile(tile, s_tiles, s_off, s_cnt, E);
+        t.two = GATED;
+        return t;
+    }
+    const int P = p.up_rows / 128, NT = p.sw_rowblocks - P, S = NT - P;
+    const int mtt = s_tiles[E] / NT;  // m-tiles of all experts
+    int g, nt;
+    if (tile < P * mtt) {
+        g = tile / P;
+        nt = tile - g * P;
+    } else {
+        const int r = tile - P * mtt;  // S > 0 here
+        g = r / S;
+        nt = P + (r - g * S);
+    }
+    int lo = 0, hi = E;  // s_tiles[lo] / NT <= g < s_tiles[hi] / NT
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_tiles[mid] <= g * NT)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const int mt = g - s_tiles[lo] / NT;
+    DecTile t;
+    t.e = lo;
+    t.nt = nt < P ? nt : nt + P;
+    t.two = nt < P;
+    t.row0 = s_off[lo] + mt * 32;
+    t.rows = min(32, s_cnt[lo] - mt * 32);
+    return t;
 }
 
 template <bool GATED, bool PAIRED>
@@ -185,10 +225,10 @@ __global__ void __launch_bounds__(DecCfg<GATED, PAIRED>::THREADS, 1)
     int pre = 0;  // stages whose weight boxes are in flight before the wait
     if (warp == 0 && lane == 0) {
         for (int tile = blockIdx.x; tile < total && pre < nst; tile += gridDim.x) {
-            const DecTile ti = decode_dec_tile(tile, s_tiles, s_off, s_cnt, E);
+            const DecTile ti = dec_tile<GATED, PAIRED>(tile, s_tiles, s_off, s_cnt, E, p);
             const int wblk = (ti.e * p.sw_rowblocks + ti.nt) * p.KB;
             const int ublk = (p.up_rows / 128) * p.KB;
-            const bool two = dec_has_second<GATED, PAIRED>(ti, p);
+            const bool two = ti.two;
             const int nxb = (ti.rows + kDecXBoxRows - 1) / kDecXBoxRows;
             for (int kb = 0; kb < p.KB && pre < nst; kb += C::KPS, ++pre) {
                 const int nk = min(C::KPS, p.KB - kb);
@@ -212,10 +252,10 @@ __global__ void __launch_bounds__(DecCfg<GATED, PAIRED>::THREADS, 1)
             uint32_t phase = 0, filled = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                const DecTile ti = decode_dec_tile(tile, s_tiles, s_off, s_cnt, E);
+                const DecTile ti = dec_tile<GATED, PAIRED>(tile, s_tiles, s_off, s_cnt, E, p);
                 const int wblk = (ti.e * p.sw_rowblocks + ti.nt) * p.KB;
                 const int ublk = (p.up_rows / 128) * p.KB;
-                const bool two = dec_has_second<GATED, PAIRED>(ti, p);
+                const bool two = ti.two;
                 const int nxb = (ti.rows + kDecXBoxRows - 1) / kDecXBoxRows;
                 for (int kb = 0; kb < p.KB; kb += C::KPS) {
                     const int nk = min(C::KPS, p.KB - kb);
@@ -272,8 +312,7 @@ __global__ void __launch_bounds__(DecCfg<GATED, PAIRED>::THREADS, 1)
             uint32_t sphase = 0, tphase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                const bool two = C::TWO && dec_has_second<GATED, PAIRED>(
-                                               decode_dec_tile(tile, s_tiles, s_off, s_cnt, E), p);
+                const bool two = C::TWO && dec_tile<GATED, PAIRED>(tile, s_tiles, s_off, s_cnt, E, p).two;
                 for (int kb = 0; kb < p.KB && ok; kb += C::KPS) {
                     const int nk = min(C::KPS, p.KB - kb);
                     if (!mbar_wait(smem_u32(&full_bar[stage]), sphase, abort_p, err, kErrTimeoutMma)) {
@@ -325,8 +364,8 @@ __global__ void __launch_bounds__(DecCfg<GATED, PAIRED>::THREADS, 1)
             const uint32_t use = (uint32_t)(it >> 1) & 1u;  // parity of this slot's use
             if (!mbar_wait(smem_u32(&mempty_bar[slot]), use ^ 1u, abort_p, err, kErrTimeoutProducer)) break;
             float* m = meta + slot * M.floats;
-            const DecTile ti = decode_dec_tile(tile, s_tiles, s_off, s_cnt, E);
-            const bool two = dec_has_second<GATED, PAIRED>(ti, p);
+            const DecTile ti = dec_tile<GATED, PAIRED>(tile, s_tiles, s_off, s_cnt, E, p);
+            const bool two = ti.two;
             const uint16_t* bias_e = p.bias + (size_t)ti.e * (GATED ? 2 * p.N_real : p.N_real);
             // bias of the tile's features: [0, 128) first row block, [128, 256) second
 #pragma unroll
@@ -370,7 +409,7 @@ __global__ void __launch_bounds__(DecCfg<GATED, PAIRED>::THREADS, 1)
             const uint32_t tpar = (uint32_t)it & 1u;
             if (!mbar_wait(smem_u32(&mfull_bar[slot]), use, abort_p, err, kErrTimeoutEpilogue)) break;
             const float* m = meta + slot * M.floats;
-            const DecTile ti = decode_dec_tile(tile, s_tiles, s_off, s_cnt, E);
+            const DecTile ti = dec_tile<GATED, PAIRED>(tile, s_tiles, s_off, s_cnt, E, p);
             const int n = ti.nt * 128 + nl;
             const bool nvalid = n < p.N_real;
             float acc[C::ACC_COLS];
@@ -457,7 +496,7 @@ __global__ void __launch_bounds__(DecCfg<GATED, PAIRED>::THREADS, 1)
                 const int slot_l = reinterpret_cast<const int*>(m)[M.slot + lane];
                 const float w_l = m[M.w + lane];
                 mbar_arrive(smem_u32(&mempty_bar[slot]));
-                const bool two = dec_has_second<GATED, PAIRED>(ti, p);
+                const bool two = ti.two;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int slot_t = __shfl_sync(0xffffffffu, slot_l, j);

@@ -48,8 +48,11 @@
 
 namespace moe {
 
+// nt: the tile's (first) weight row block; two: whether a second row block,
+// up_rows / 128 further on, is part of it (decode tiles)
 struct MxTile {
     int e, nt, mt, row0, rows;
+    bool two;
 };
 
 // Tile -> (expert, n-tile, m-tile), tiles ordered expert, n-tile, m-tile.
@@ -71,6 +74,7 @@ __device__ __forceinline__ MxTile mx_tile(int tile, const int* s_tiles, const in
     t.mt = local - t.nt * mtc;
     t.row0 = s_off[lo] + t.mt * BM;
     t.rows = min(BM, s_cnt[lo] - t.mt * BM);
+    t.two = false;
     return t;
 }
 
@@ -410,20 +414,24 @@ __global__ void __launch_bounds__(MxCfg<GATED, FP4W>::THREADS, 1)
 }
 
 // ====================================================================== decode
-template <bool GATED, bool FP4W>
+// GATED: gate and up row blocks of one n-tile per K step.  PAIRED (down GEMM
+// only): w2 row blocks nt and nt + up_rows/128 per K step, as in the 128x128
+// decode down GEMM; otherwise one row block, KPS K blocks per stage.
+template <bool GATED, bool FP4W, bool PAIRED = false>
 struct MxDecCfg {
-    static constexpr int BT = 32;  // token rows per tile (MMA N)
-    static constexpr int W_BYTES = (GATED ? 2 : 1) * 128 * 128;
+    static constexpr bool TWO = GATED || PAIRED;  // two weight row blocks per K step
+    static constexpr int BT = 32;                 // token rows per tile (MMA N)
+    static constexpr int W_BYTES = (TWO ? 2 : 1) * 128 * 128;
     static constexpr int X_BYTES = BT * 128;
     // K blocks per ring stage (the ring's round trip is paid once per stage);
     // a stage holds the KPS weight blocks, then the KPS token-row blocks
-    static constexpr int KPS = GATED ? MOE_MX_DEC_KPS_GATEUP : MOE_MX_DEC_KPS_DOWN;
+    static constexpr int KPS = GATED ? MOE_MX_DEC_KPS_GATEUP : (PAIRED ? 1 : MOE_MX_DEC_KPS_DOWN);
     static constexpr int STAGE_BYTES = KPS * (W_BYTES + X_BYTES);
     static constexpr int W_TX = FP4W ? W_BYTES / 2 : W_BYTES;  // packed bytes of 4-bit weight boxes
-    static constexpr int SF_KB = (GATED ? 3 : 2) * kMxAtomBytes;  // atoms of one K block: weight block(s), token tile
+    static constexpr int SF_KB = (TWO ? 3 : 2) * kMxAtomBytes;  // atoms of one K block: weight block(s), token tile
     static constexpr int SF_BYTES = KPS * SF_KB;
     static constexpr int MAX_STAGES = 16 / KPS;
-    static constexpr int ACC_COLS = GATED ? 2 * BT : BT;
+    static constexpr int ACC_COLS = TWO ? 2 * BT : BT;
     static constexpr int NACC = 4;  // accumulator buffers
     static constexpr int SF_COL0 = 256;
     static constexpr int SF_STRIDE = 16 * KPS;  // TMEM scale columns of one stage (16 per K block)
@@ -437,11 +445,53 @@ struct MxDecCfg {
     static_assert(SF_COL0 + MAX_STAGES * SF_STRIDE <= TMEM_COLS, "scale ring does not fit in TMEM");
 };
 
-template <bool GATED, bool FP4W>
-__global__ void __launch_bounds__(MxDecCfg<GATED, FP4W>::THREADS, 1)
+// Decode tile -> (expert, row block(s), m-tile): the order of mx_tile, except
+// for paired down tiles (P = up_rows / 128 > 0), where of the nt = RB - P
+// n-tiles of an m-tile the first P take w2 row blocks j and j + P and the
+// other RB - 2P one block each, every m-tile's paired tiles listed before all
+// the one-block ones (the layout of the 128x128 decode down GEMM's list).
+template <bool GATED, bool PAIRED, int BM>
+__device__ __forceinline__ MxTile mx_dec_tile(int tile, const int* s_tiles, const int* s_off, const int* s_cnt, int E,
+                                              const MxGemmParams& p) {
+    if (!PAIRED) {
+        MxTile t = mx_tile<BM>(tile, s_tiles, s_off, s_cnt, E);
+        t.two = GATED;
+        return t;
+    }
+    const int P = p.up_rows / 128, NT = p.nt, S = NT - P;
+    const int mtt = s_tiles[E] / NT;  // m-tiles of all experts
+    int g, nt;
+    if (tile < P * mtt) {
+        g = tile / P;
+        nt = tile - g * P;
+    } else {
+        const int r = tile - P * mtt;  // S > 0 here
+        g = r / S;
+        nt = P + (r - g * S);
+    }
+    int lo = 0, hi = E;  // s_tiles[lo] / NT <= g < s_tiles[hi] / NT
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_tiles[mid] <= g * NT)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    MxTile t;
+    t.e = lo;
+    t.mt = g - s_tiles[lo] / NT;
+    t.nt = nt < P ? nt : nt + P;
+    t.two = nt < P;
+    t.row0 = s_off[lo] + t.mt * BM;
+    t.rows = min(BM, s_cnt[lo] - t.mt * BM);
+    return t;
+}
+
+template <bool GATED, bool FP4W, bool PAIRED>
+__global__ void __launch_bounds__(MxDecCfg<GATED, FP4W, PAIRED>::THREADS, 1)
     moe_gemm_mx_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                               const MxGemmParams p, const int nst) {
-    using C = MxDecCfg<GATED, FP4W>;
+    using C = MxDecCfg<GATED, FP4W, PAIRED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sf_smem = smem + nst * C::STAGE_BYTES;
@@ -456,7 +506,7 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, FP4W>::THREADS, 1)
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ int s_tiles[kMaxExperts + 1], s_off[kMaxExperts + 1], s_cnt[kMaxExperts];
-    __shared__ float s_bias[2][GATED ? 256 : 128];
+    __shared__ float s_bias[2][C::TWO ? 256 : 128];
     __shared__ int s_slot[2][32];
     __shared__ float s_w[2][32];
 
@@ -505,11 +555,12 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, FP4W>::THREADS, 1)
             int stage = 0;
             uint32_t phase = 0, filled = 0;
             bool ok = true;
-            const int ublk = GATED ? (p.up_rows / 128) * p.KB : 0;
+            const int ublk = (p.up_rows / 128) * p.KB;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                const MxTile ti = mx_tile<C::BT>(tile, s_tiles, s_off, s_cnt, E);
+                const MxTile ti = mx_dec_tile<GATED, PAIRED, C::BT>(tile, s_tiles, s_off, s_cnt, E, p);
                 const int mtid = s_tiles[ti.e] / p.nt + ti.mt;
                 const int wblk = (ti.e * p.sw_rowblocks + ti.nt) * p.KB;
+                const bool two = C::TWO && ti.two;
                 const int nxb = (ti.rows + kDecXBoxRows - 1) / kDecXBoxRows;
                 const uint8_t* sa = p.sa + (size_t)mtid * p.KB * kMxAtomBytes;
                 for (int kb0 = 0; kb0 < p.KB; kb0 += C::KPS) {
@@ -519,7 +570,9 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, FP4W>::THREADS, 1)
                         break;
                     }
                     const uint32_t fb = smem_u32(&full_bar[stage]);
-                    mbar_arrive_expect_tx(fb, nk * (C::W_TX + nxb * kDecXBoxRows * 128 + C::SF_KB));
+                    // one weight box and one scale atom fewer when a paired tile has no second block
+                    const int miss = C::TWO && !two ? C::W_TX / 2 + kMxAtomBytes : 0;
+                    mbar_arrive_expect_tx(fb, nk * (C::W_TX + nxb * kDecXBoxRows * 128 + C::SF_KB - miss));
                     for (int i = 0; i < nk; ++i) {
                         const int kb = kb0 + i;
                         const uint32_t w_dst = smem_u32(smem + stage * C::STAGE_BYTES + i * C::W_BYTES);
@@ -528,7 +581,7 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, FP4W>::THREADS, 1)
                         const uint32_t sf_dst = smem_u32(sf_smem + stage * C::SF_BYTES + i * C::SF_KB);
                         tma_load_2d(w_dst, &tmW, 0, (wblk + kb) * 128, fb);
                         bulk_load(sf_dst, p.sw + (size_t)(wblk + kb) * kMxAtomBytes, kMxAtomBytes, fb);
-                        if (GATED) {
+                        if (two) {
                             tma_load_2d(w_dst + 128 * 128, &tmW, 0, (wblk + ublk + kb) * 128, fb);
                             bulk_load(sf_dst + kMxAtomBytes, p.sw + (size_t)(wblk + ublk + kb) * kMxAtomBytes,
                                       kMxAtomBytes, fb);
@@ -537,7 +590,7 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, FP4W>::THREADS, 1)
                         // memory for the other token columns, whose results are never stored
                         for (int b = 0; b < nxb; ++b)
                             tma_load_2d(x_dst + b * kDecXBoxRows * 128, &tmX, kb * 128, ti.row0 + b * kDecXBoxRows, fb);
-                        bulk_load(sf_dst + (GATED ? 2 : 1) * kMxAtomBytes, sa + (size_t)kb * kMxAtomBytes,
+                        bulk_load(sf_dst + (C::TWO ? 2 : 1) * kMxAtomBytes, sa + (size_t)kb * kMxAtomBytes,
                                   kMxAtomBytes, fb);
                     }
                     filled |= 1u << stage;
@@ -570,6 +623,7 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, FP4W>::THREADS, 1)
             uint32_t sphase = 0, aphase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const bool two = C::TWO && mx_dec_tile<GATED, PAIRED, C::BT>(tile, s_tiles, s_off, s_cnt, E, p).two;
                 if (!mbar_wait(smem_u32(&dempty_bar[buf]), aphase ^ 1u, abort_p, err, kErrTimeoutMma)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(buf * C::ACC_COLS);
@@ -589,15 +643,15 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, FP4W>::THREADS, 1)
                         const uint32_t tsf = tmem_base + (uint32_t)(C::SF_COL0 + stage * C::SF_STRIDE + 16 * i);
                         // SFA: gate (or only) block [tsf, tsf+4), up block [tsf+4, tsf+8); SFB: tokens [tsf+8, ...)
                         tmem_cp_atom(tsf, sf_src);
-                        if (GATED) tmem_cp_atom(tsf + 4, sf_src + kMxAtomBytes);
-                        tmem_cp_atom(tsf + 8, sf_src + (GATED ? 2 : 1) * kMxAtomBytes);
+                        if (two) tmem_cp_atom(tsf + 4, sf_src + kMxAtomBytes);
+                        tmem_cp_atom(tsf + 8, sf_src + (C::TWO ? 2 : 1) * kMxAtomBytes);
 #pragma unroll
                         for (int k4 = 0; k4 < 4; ++k4) {
                             const uint64_t xd = smem_desc_sw128(x_base + 32 * k4);
                             const uint32_t id = idesc_sf_id(C::IDESC, (uint32_t)k4);
                             const uint32_t acc = (kb | k4) != 0 ? 1u : 0u;
                             mma_mx(d, smem_desc_sw128(w_base + 32 * k4), xd, id, tsf, tsf + 8, acc);
-                            if (GATED)
+                            if (two)
                                 mma_mx(d + C::BT, smem_desc_sw128(w_base + 128 * 128 + 32 * k4), xd, id, tsf + 4,
                                        tsf + 8, acc);
                         }
@@ -626,12 +680,14 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, FP4W>::THREADS, 1)
             const int slot = it & 1;
             const uint32_t use = (uint32_t)(it >> 1) & 1u;
             if (!mbar_wait(smem_u32(&mempty_bar[slot]), use ^ 1u, abort_p, err, kErrTimeoutProducer)) break;
-            const MxTile ti = mx_tile<C::BT>(tile, s_tiles, s_off, s_cnt, E);
+            const MxTile ti = mx_dec_tile<GATED, PAIRED, C::BT>(tile, s_tiles, s_off, s_cnt, E, p);
             const uint16_t* bias_e = p.bias + (size_t)ti.e * (GATED ? 2 * p.N_real : p.N_real);
+            // bias of the tile's features: [0, 128) first row block, [128, 256) second
 #pragma unroll
-            for (int c = lane; c < (GATED ? 256 : 128); c += 32) {
-                const int n = ti.nt * 128 + (c & 127);
-                s_bias[slot][c] = n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + (c >> 7) * p.N_real + n)) : 0.f;
+            for (int c = lane; c < (C::TWO ? 256 : 128); c += 32) {
+                const int n = ti.nt * 128 + (c & 127) + (GATED ? 0 : (c >> 7) * p.up_rows);
+                s_bias[slot][c] =
+                    n < p.N_real ? bf16_bits_to_f32(__ldg(bias_e + (GATED ? (c >> 7) * p.N_real : 0) + n)) : 0.f;
             }
             if (!GATED) {
                 const int st = __ldg(p.perm + min(ti.row0 + lane, p.R - 1));
@@ -652,10 +708,10 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, FP4W>::THREADS, 1)
             const uint32_t use = (uint32_t)(it >> 1) & 1u;
             if (!mbar_wait(smem_u32(&dfull_bar[buf]), aphase, abort_p, err, kErrTimeoutEpilogue)) break;
             tc_fence_after();
-            float acc[C::ACC_COLS];  // column j: token j (gate/up: gate [0, 32), up [32, 64))
+            float acc[C::ACC_COLS];  // column j: token j (gate/up: gate [0, 32), up [32, 64); paired likewise)
             {
                 const uint32_t tcol = t_lane + (uint32_t)(buf * C::ACC_COLS);
-                if (GATED) {
+                if (C::TWO) {
                     uint32_t r[64];
                     tmem_ld64(tcol, r);
 #pragma unroll
@@ -675,15 +731,15 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, FP4W>::THREADS, 1)
                 aphase ^= 1u;
             }
             if (!mbar_wait(smem_u32(&mfull_bar[slot]), use, abort_p, err, kErrTimeoutEpilogue)) break;
-            const MxTile ti = mx_tile<C::BT>(tile, s_tiles, s_off, s_cnt, E);
+            const MxTile ti = mx_dec_tile<GATED, PAIRED, C::BT>(tile, s_tiles, s_off, s_cnt, E, p);
             const int n = ti.nt * 128 + nl;
             {
                 const float bg = s_bias[slot][nl];
-                const float bu = GATED ? s_bias[slot][GATED ? 128 + nl : 0] : 0.f;
+                const float bu = C::TWO ? s_bias[slot][C::TWO ? 128 + nl : 0] : 0.f;
 #pragma unroll
                 for (int j = 0; j < C::BT; ++j) {
                     acc[j] += bg;
-                    if (GATED) acc[C::BT + j] += bu;
+                    if (C::TWO) acc[C::BT + j] += bu;
                 }
             }
             if (GATED) {
@@ -715,11 +771,15 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, FP4W>::THREADS, 1)
                 const int slot_l = s_slot[slot][lane];
                 const float w_l = s_w[slot][lane];
                 mbar_arrive(smem_u32(&mempty_bar[slot]));
+                const bool two = C::TWO && ti.two;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int slot_t = __shfl_sync(0xffffffffu, slot_l, j);
                     const float w = __shfl_sync(0xffffffffu, w_l, j);
-                    if (j < ti.rows) p.part[(size_t)slot_t * p.ldp + n] = w * acc[j];
+                    if (j < ti.rows) {
+                        p.part[(size_t)slot_t * p.ldp + n] = w * acc[j];
+                        if (two) p.part[(size_t)slot_t * p.ldp + n + p.up_rows] = w * acc[C::BT + j];
+                    }
                 }
             }
         }
@@ -747,15 +807,15 @@ static cudaError_t launch_mx_prefill(const CUtensorMap& tmX, const CUtensorMap& 
 
 // The stage ring takes the shared memory the kernel's static arrays leave, up
 // to `max_stages` stages.
-template <bool GATED, bool FP4W>
+template <bool GATED, bool FP4W, bool PAIRED>
 static cudaError_t launch_mx_decode(const CUtensorMap& tmX, const CUtensorMap& tmW, const MxGemmParams& p, int grid,
                                     int max_stages, cudaStream_t st) {
-    using C = MxDecCfg<GATED, FP4W>;
+    using C = MxDecCfg<GATED, FP4W, PAIRED>;
     int dev = 0, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     cudaFuncAttributes fa;
-    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, moe_gemm_mx_decode_kernel<GATED, FP4W>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, moe_gemm_mx_decode_kernel<GATED, FP4W, PAIRED>);
     if (e != cudaSuccess) return e;
     const long long room = (long long)optin - (long long)fa.sharedSizeBytes - 1024;
     int nst = (int)(room / (C::STAGE_BYTES + C::SF_BYTES));
@@ -763,10 +823,10 @@ static cudaError_t launch_mx_decode(const CUtensorMap& tmX, const CUtensorMap& t
     if (nst > C::MAX_STAGES) nst = C::MAX_STAGES;
     if (nst < 2) return cudaErrorInvalidConfiguration;
     const size_t smem = (size_t)nst * (C::STAGE_BYTES + C::SF_BYTES) + 1024;
-    e = cudaFuncSetAttribute(moe_gemm_mx_decode_kernel<GATED, FP4W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(moe_gemm_mx_decode_kernel<GATED, FP4W, PAIRED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(moe_gemm_mx_decode_kernel<GATED, FP4W>, dim3(grid), dim3(C::THREADS), smem, st, tmX, tmW, p,
+    return launch_pdl(moe_gemm_mx_decode_kernel<GATED, FP4W, PAIRED>, dim3(grid), dim3(C::THREADS), smem, st, tmX, tmW, p,
                       nst);
 }
 
@@ -774,8 +834,9 @@ template <bool FP4W>
 static cudaError_t launch_mx(bool gated, bool decode, const CUtensorMap& tmX, const CUtensorMap& tmW,
                              const MxGemmParams& p, int grid, cudaStream_t st) {
     if (decode)
-        return gated ? launch_mx_decode<true, FP4W>(tmX, tmW, p, grid, kDecStagesGateUp, st)
-                     : launch_mx_decode<false, FP4W>(tmX, tmW, p, grid, kDecStagesDown, st);
+        return gated            ? launch_mx_decode<true, FP4W, false>(tmX, tmW, p, grid, kDecStagesGateUp, st)
+               : p.up_rows != 0 ? launch_mx_decode<false, FP4W, true>(tmX, tmW, p, grid, kDecStagesGateUp, st)
+                                : launch_mx_decode<false, FP4W, false>(tmX, tmW, p, grid, kDecStagesDown, st);
     return gated ? launch_mx_prefill<true, FP4W>(tmX, tmW, p, grid, st)
                  : launch_mx_prefill<false, FP4W>(tmX, tmW, p, grid, st);
 }

@@ -111,7 +111,8 @@ struct MxGemmParams {
     int E, R, KB;          // K / 128
     int N_real;            // gate/up GEMM: I; down GEMM: H
     int sw_rowblocks;      // rows of one expert's weight matrix / 128
-    int up_rows;           // gate/up GEMM: Ip (row offset of the up half)
+    int up_rows;           // rows from a tile's first weight row block to its second: gate/up GEMM Ip
+                           // (the up half); paired decode down GEMM ceil(Hp/256)*128; else 0
     int nt;                // n-tiles per m-tile (tiles[e] = nt * m-tiles of the experts before e)
     const int32_t* count;
     const int32_t* offset;

@@ -66,12 +66,14 @@ def full_check(moe, layer: Layer, n_sample: int | None = None, upload: bool = Tr
     bm = 32 if decode else 128
     assert st[3] == bm
     mt = (p["count"] + bm - 1) // bm
-    # down GEMM: 256-feature tiles (two w2 row blocks) at prefill, and at decode unless one-block
-    # tiles for the min(E, T*k) experts that can be active would not fill the SMs
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    single = decode and min(E, T * k) * (layer.Hp // 128) <= sms
-    nt2 = layer.Hp // 128 if single else (layer.Hp // 128 + 1) // 2
-    assert st[1] == mt.sum() * (layer.Ip // 128) and st[2] == mt.sum() * nt2
+    # down GEMM: 256-feature tiles (two w2 row blocks) at prefill; at decode P of the RB n-tiles
+    # of an m-tile pair two row blocks and RB - 2P take one (P chosen at launch, 0 <= P <= RB/2)
+    RB = layer.Hp // 128
+    assert st[1] == mt.sum() * (layer.Ip // 128)
+    if decode:
+        assert st[2] % mt.sum() == 0 and RB - RB // 2 <= st[2] // mt.sum() <= RB
+    else:
+        assert st[2] == mt.sum() * ((RB + 1) // 2)
     # x quantisation: bit-exact codes and scales in every permuted row
     xq, sx = oracle.quant_rows_bf16(layer.x)
     tok_of_row = p["perm"] // k
