@@ -159,6 +159,20 @@ def test_ragged_hidden_and_intermediate(moe):
     full_check(moe, _adhoc("ragged", 37, 200, 136, 5, 3))
 
 
+# Decode-sized batches whose one-block down tiles would outnumber the SMs: the
+# down GEMM takes two w2 row blocks (j and j + RB/2) per tile; with an even
+# block count every tile is paired, with an odd one each m-tile also has one
+# one-block tile, listed after all the paired ones.
+PAIRED_DOWN_SHAPES = [("paired_even_blocks", 48, 256, 128), ("paired_odd_blocks", 32, 384, 64)]
+
+
+@pytest.mark.parametrize("name,T,H,E", PAIRED_DOWN_SHAPES, ids=lambda v: v if isinstance(v, str) else None)
+def test_decode_paired_down_tiles(moe, name, T, H, E):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert min(E, T * 4) * ((H + 127) // 128) > sms  # the shape takes the paired tiles
+    full_check(moe, _adhoc(name, T, H, 256, E, 4))
+
+
 def test_all_tokens_to_two_experts_multi_tile(moe):
     # experts 0 and 1 get every token (3 M tiles each: 128 + 128 + 44 rows); experts 2..7 get none
     rb = np.array([8.0, 8.0, 0, 0, 0, 0, 0, 0], np.float32)

@@ -159,6 +159,13 @@ def test_mx_prefill_odd_block_count(moe):
     full_check_mx(moe, adhoc("odd_blocks", 600, 384, 200, 4, 2), n_sample=64)
 
 
+@pytest.mark.parametrize("name,T,H,E", [("paired_even_blocks", 48, 256, 128), ("paired_odd_blocks", 32, 384, 64)],
+                         ids=lambda v: v if isinstance(v, str) else None)
+def test_mx_decode_paired_down_tiles(moe, name, T, H, E):
+    # the decode down GEMM's paired w2 row blocks (RB even: every tile; RB odd: plus one one-block tile)
+    full_check_mx(moe, adhoc(name, T, H, 256, E, 4))
+
+
 def test_mx_many_tokens_router_scan(moe):
     full_check_mx(moe, adhoc("many_tokens", 2500, 256, 256, 8, 2), n_sample=48)
 

@@ -61,6 +61,13 @@ def test_mx4_tiny_layer_all_tokens(moe):
     full_check_mx(moe, Layer(synth.config("tiny"), fp4=True))
 
 
+@pytest.mark.parametrize("name,T,H,E", [("paired_even_blocks", 48, 256, 128), ("paired_odd_blocks", 32, 384, 64)],
+                         ids=lambda v: v if isinstance(v, str) else None)
+def test_mx4_decode_paired_down_tiles(moe, name, T, H, E):
+    # the decode down GEMM's paired w2 row blocks with E2M1 weight boxes
+    full_check_mx(moe, adhoc4(name, T, H, 256, E, 4))
+
+
 def test_mx4_single_token(moe):
     full_check_mx(moe, adhoc4("one_token", 1, 256, 256, 8, 2))
 
