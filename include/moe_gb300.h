@@ -78,7 +78,9 @@ typedef struct {
     size_t offset;     /* int32 [E+1]   first row of each expert (exclusive scan of count) */
     size_t chunk_base; /* int32 [ceil(T/256), E] first row of each (chunk, expert) */
     size_t tiles1;     /* int32 [E+1]   first gate/up GEMM tile of each expert */
-    size_t tiles2;     /* int32 [E+1]   first down GEMM tile of each expert */
+    size_t tiles2;     /* int32 [E+1]   down GEMM tiles before each expert: its n-tiles per m-tile times
+                          the m-tiles of the experts before it (a count prefix; at decode sizes the
+                          kernel lists every m-tile's two-block tiles before the one-block ones) */
     size_t topk_idx;   /* int32 [T, top_k] selected experts, ascending */
     size_t topk_w;     /* float [T, top_k] softmax weights before bf16 rounding */
     size_t topk_wb;    /* bf16  [T, top_k] routing weights used by the layer */
