@@ -242,6 +242,23 @@ def test_graphed_layer_matches_eager(moe):
         assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
 
 
+@pytest.mark.parametrize("name,T,H,E,k", [("graph_decode", 48, 256, 128, 4), ("graph_prefill", 600, 384, 4, 2)],
+                         ids=lambda v: v if isinstance(v, str) else None)
+def test_graphed_layer_matches_eager_both_regimes(moe, name, T, H, E, k):
+    # decode-sized (paired down tiles) and prefill-sized (two MMA issuers) batches through one graph
+    cfg = synth.LayerConfig(name, T, H, 256, E, k, 11, "normal", "normal")
+    layer = Layer(cfg, x=synth.x_rows(cfg)).to_device()  # no oracle here: any ties resolve alike
+    ml = moe.MoeLayer(layer.d_rw, layer.d_rb, layer.d_w13, layer.d_s13, layer.d_b13, layer.d_w2, layer.d_s2,
+                      layer.d_b2, layer.k)
+    g = ml.graphed(layer.T)
+    for x in (layer.d_x, torch.flip(layer.d_x, dims=[0]).contiguous()):
+        ref = ml(x)
+        g.x.copy_(x)
+        got = g()
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+
+
 def test_repeated_calls_are_bit_identical(moe):
     layer = Layer(synth.config("tiny")).to_device()
     a, _, ws = layer.run_gpu()

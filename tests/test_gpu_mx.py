@@ -170,6 +170,25 @@ def test_mx_many_tokens_router_scan(moe):
     full_check_mx(moe, adhoc("many_tokens", 2500, 256, 256, 8, 2), n_sample=48)
 
 
+@pytest.mark.parametrize("fp4", [False, True], ids=["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("name,T,H,E", [("graph_decode", 48, 256, 128), ("graph_prefill", 600, 384, 4)],
+                         ids=lambda v: v if isinstance(v, str) else None)
+def test_mx_graphed_layer_matches_eager(moe, name, T, H, E, fp4):
+    # one CUDA-graph replay (the five kernels with their programmatic dependencies) gives the
+    # eager call's bits, for decode-sized (paired down tiles) and prefill-sized batches
+    cfg = synth.LayerConfig(name, T, H, 256, E, 4 if E > 4 else 2, 11, "normal", "normal")
+    layer = Layer(cfg, x=synth.x_rows(cfg), mx=True, fp4=fp4).to_device()  # no oracle here
+    ml = moe.MoeLayer(layer.d_rw, layer.d_rb, layer.d_w13, layer.d_s13, layer.d_b13, layer.d_w2, layer.d_s2,
+                      layer.d_b2, layer.k)
+    g = ml.graphed(layer.T)
+    for x in (layer.d_x, torch.flip(layer.d_x, dims=[0]).contiguous()):
+        ref = ml(x)
+        g.x.copy_(x)
+        got = g()
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+
+
 def test_mx_repeated_calls_are_bit_identical(moe):
     layer = Layer(synth.config("tiny"), mx=True).to_device()
     a, _, ws = layer.run_gpu()
