@@ -1,4 +1,4 @@
-"""Expert-parallel dispatch / combine plans with two gloo ranks on the CPU.
+"""Expert-parallel dispatch / combine plans with two and three gloo ranks on the CPU.
 
 Each rank routes its own token batch with the oracle (router, permutation, 1x128
 x quantisation), dispatches its permuted rows to the experts' owners with
@@ -95,8 +95,8 @@ def _rank(rank: int, world: int, port: int, q):
         dist.destroy_process_group()
 
 
-def test_two_ranks_dispatch_and_combine_equal_one_rank():
-    world = 2
+@pytest.mark.parametrize("world", [2, 3])
+def test_ranks_dispatch_and_combine_equal_one_rank(world):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
